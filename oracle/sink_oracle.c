@@ -124,6 +124,16 @@ static void row_backward(const problem_t* P, const double* v, const double* dout
     for (int t = 0; t <= n; ++t) dz[t] = p[t] * (u[t] - c);
 }
 
+/* Sequence index of every token (tokens outside [0, T) do not occur). */
+static int* token_seq(const problem_t* P) {
+    const int T = P->cu[P->nseq];
+    int* ts = (int*)malloc(sizeof(int) * (size_t)(T > 0 ? T : 1));
+    if (!ts) return NULL;
+    for (int s = 0; s < P->nseq; ++s)
+        for (int t = P->cu[s]; t < P->cu[s + 1]; ++t) ts[t] = s;
+    return ts;
+}
+
 int sink_oracle_forward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv, int d,
                         double scale, int causal, int window, int row_begin, int row_end,
                         const double* q, const double* k, const double* v, const double* sinks,
@@ -133,8 +143,11 @@ int sink_oracle_forward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv, 
     if (!q || !k || !v || !sinks || !o || !lse) return -1;
     const int T = cu_seqlens[nseq];
     const int Lmax = longest(&P);
-    const int nunits = nseq * h_q;
+    int* ts = token_seq(&P);
+    if (!ts) return -1;
     int bad = 0;
+    /* rows are independent: one unit = one (token, query head) row */
+    const long long nrows = (long long)T * h_q;
 #pragma omp parallel
     {
         double* z = (double*)malloc(sizeof(double) * (size_t)(Lmax + 1));
@@ -143,34 +156,43 @@ int sink_oracle_forward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv, 
 #pragma omp atomic write
             bad = 1;
         } else {
-#pragma omp for schedule(dynamic, 1)
-            for (int unit = 0; unit < nunits; ++unit) {
-                const int s = unit / h_q, h = unit % h_q;
-                const int base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+#pragma omp for schedule(dynamic, 64)
+            for (long long r = 0; r < nrows; ++r) {
+                const int t = (int)(r / h_q), h = (int)(r % h_q);
+                const int s = ts[t], base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+                const int i = t - base;
+                if (i < row_begin || i >= row_end) continue;
                 const int hk = h / (h_q / h_kv);
-                const int i_lo = row_begin > 0 ? row_begin : 0;
-                const int i_hi = row_end < L ? row_end : L;
-                for (int i = i_lo; i < i_hi; ++i) {
-                    int j0, j1;
-                    allowed_keys(&P, i, L, &j0, &j1);
-                    const double l = row_softmax(&P, q, k, sinks, base, h, i, j0, j1, z, p);
-                    /* output = probs_content @ V: the sink column is dropped */
-                    double* oi = o + ((size_t)(base + i) * h_q + h) * d;
-                    for (int c = 0; c < d; ++c) oi[c] = 0.0;
-                    for (int t = 0; t < j1 - j0; ++t) {
-                        const double* vj = v + ((size_t)(base + j0 + t) * h_kv + hk) * d;
-                        for (int c = 0; c < d; ++c) oi[c] += p[t] * vj[c];
-                    }
-                    lse[(size_t)h * T + base + i] = l;
+                int j0, j1;
+                allowed_keys(&P, i, L, &j0, &j1);
+                const double l = row_softmax(&P, q, k, sinks, base, h, i, j0, j1, z, p);
+                /* output = probs_content @ V: the sink column is dropped */
+                double* oi = o + ((size_t)t * h_q + h) * d;
+                for (int c = 0; c < d; ++c) oi[c] = 0.0;
+                for (int u = 0; u < j1 - j0; ++u) {
+                    const double* vj = v + ((size_t)(base + j0 + u) * h_kv + hk) * d;
+                    for (int c = 0; c < d; ++c) oi[c] += p[u] * vj[c];
                 }
+                lse[(size_t)h * T + t] = l;
             }
         }
         free(z);
         free(p);
     }
+    free(ts);
     return bad ? -1 : 0;
 }
 
+/*
+ * Backward in two passes, each a plain loop over independent outputs.
+ * Pass 1, per row (i, h): the combined row's softmax p and the chain-rule
+ * gradient dz = p (u - c) (row_backward). It yields dq_i = scale sum_j dz_ij k_j,
+ * the row's term dz_sink of dL/dS_h, and keeps the row's logsumexp and c_i.
+ * Pass 2, per key (j, key/value head): dk_j = scale sum dz_ij q_i and
+ * dv_j = sum p_ij dO_i over every (query head of the group, row that sees j),
+ * with p_ij = exp(z_ij - logsumexp_i) and dz_ij = p_ij (u_ij - c_i) evaluated
+ * from the kept per-row quantities.
+ */
 int sink_oracle_backward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv, int d,
                          double scale, int causal, int window, int row_begin, int row_end,
                          const double* q, const double* k, const double* v, const double* sinks,
@@ -182,17 +204,21 @@ int sink_oracle_backward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv,
     const int T = cu_seqlens[nseq];
     const int g = h_q / h_kv;
     const int Lmax = longest(&P);
+    int* ts = token_seq(&P);
+    /* per (query head, token): logsumexp, c = sum_t p_t u_t, sink term, in-range flag */
+    double* row_lse = (double*)calloc((size_t)h_q * (T > 0 ? T : 1), sizeof(double));
+    double* row_c = (double*)calloc((size_t)h_q * (T > 0 ? T : 1), sizeof(double));
+    double* row_sink = (double*)calloc((size_t)h_q * (T > 0 ? T : 1), sizeof(double));
+    if (!ts || !row_lse || !row_c || !row_sink) {
+        free(ts);
+        free(row_lse);
+        free(row_c);
+        free(row_sink);
+        return -1;
+    }
     memset(dq, 0, sizeof(double) * (size_t)T * h_q * d);
-    memset(dk, 0, sizeof(double) * (size_t)T * h_kv * d);
-    memset(dv, 0, sizeof(double) * (size_t)T * h_kv * d);
-    /* per-(sequence, query head) partial sums of dL/dS_h, added in a fixed order
-     * at the end so the result does not depend on the thread count */
-    double* part = (double*)calloc((size_t)(nseq > 0 ? nseq : 1) * h_q, sizeof(double));
-    if (!part) return -1;
-    /* one unit = (sequence, key/value head): dk and dv rows of a unit are
-     * written by that unit only */
-    const int nunits = nseq * h_kv;
     int bad = 0;
+    const long long nrows = (long long)T * h_q;
 #pragma omp parallel
     {
         double* z = (double*)malloc(sizeof(double) * (size_t)(Lmax + 1));
@@ -203,40 +229,29 @@ int sink_oracle_backward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv,
 #pragma omp atomic write
             bad = 1;
         } else {
-#pragma omp for schedule(dynamic, 1)
-            for (int unit = 0; unit < nunits; ++unit) {
-                const int s = unit / h_kv, hk = unit % h_kv;
-                const int base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
-                const int i_lo = row_begin > 0 ? row_begin : 0;
-                const int i_hi = row_end < L ? row_end : L;
-                for (int h = hk * g; h < (hk + 1) * g; ++h) {
-                    double dsink = 0.0;
-                    for (int i = i_lo; i < i_hi; ++i) {
-                        int j0, j1;
-                        allowed_keys(&P, i, L, &j0, &j1);
-                        const int n = j1 - j0;
-                        row_softmax(&P, q, k, sinks, base, h, i, j0, j1, z, p);
-                        row_backward(&P, v, dout, base, h, i, j0, j1, p, u, dz);
-                        const double* qi = q + ((size_t)(base + i) * h_q + h) * d;
-                        const double* doi = dout + ((size_t)(base + i) * h_q + h) * d;
-                        double* dqi = dq + ((size_t)(base + i) * h_q + h) * d;
-                        for (int t = 0; t < n; ++t) {
-                            const size_t kv_off = ((size_t)(base + j0 + t) * h_kv + hk) * d;
-                            const double* kj = k + kv_off;
-                            double* dkj = dk + kv_off;
-                            double* dvj = dv + kv_off;
-                            /* S_ij = scale * q_i . k_j */
-                            const double gs = scale * dz[t];
-                            for (int c = 0; c < d; ++c) {
-                                dqi[c] += gs * kj[c];
-                                dkj[c] += gs * qi[c];
-                                dvj[c] += p[t] * doi[c];
-                            }
-                        }
-                        dsink += dz[n];
-                    }
-                    part[(size_t)s * h_q + h] = dsink;
+#pragma omp for schedule(dynamic, 64)
+            for (long long r = 0; r < nrows; ++r) {
+                const int t = (int)(r / h_q), h = (int)(r % h_q);
+                const int s = ts[t], base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+                const int i = t - base;
+                if (i < row_begin || i >= row_end) continue;
+                const int hk = h / g;
+                int j0, j1;
+                allowed_keys(&P, i, L, &j0, &j1);
+                const int n = j1 - j0;
+                const double l = row_softmax(&P, q, k, sinks, base, h, i, j0, j1, z, p);
+                row_backward(&P, v, dout, base, h, i, j0, j1, p, u, dz);
+                double c = 0.0;
+                for (int m = 0; m < n; ++m) c += p[m] * u[m];
+                double* dqi = dq + ((size_t)t * h_q + h) * d;
+                for (int m = 0; m < n; ++m) {
+                    /* S_ij = scale * q_i . k_j */
+                    const double* kj = k + ((size_t)(base + j0 + m) * h_kv + hk) * d;
+                    for (int e = 0; e < d; ++e) dqi[e] += scale * dz[m] * kj[e];
                 }
+                row_lse[(size_t)h * T + t] = l;
+                row_c[(size_t)h * T + t] = c;
+                row_sink[(size_t)h * T + t] = dz[n];
             }
         }
         free(z);
@@ -244,12 +259,47 @@ int sink_oracle_backward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv,
         free(u);
         free(dz);
     }
+    /* pass 2: one unit = one (token, key/value head) key row */
+    const long long nkeys = (long long)T * h_kv;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (long long r = 0; r < nkeys; ++r) {
+        const int t = (int)(r / h_kv), hk = (int)(r % h_kv);
+        const int s = ts[t], base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+        const int j = t - base;
+        const size_t kv_off = ((size_t)t * h_kv + hk) * d;
+        const double* kj = k + kv_off;
+        const double* vj = v + kv_off;
+        double* dkj = dk + kv_off;
+        double* dvj = dv + kv_off;
+        for (int e = 0; e < d; ++e) dkj[e] = dvj[e] = 0.0;
+        for (int h = hk * g; h < (hk + 1) * g; ++h) {
+            for (int i = 0; i < L; ++i) {
+                if (i < row_begin || i >= row_end) continue;
+                int j0, j1;
+                allowed_keys(&P, i, L, &j0, &j1);
+                if (j < j0 || j >= j1) continue;
+                const size_t ri = (size_t)h * T + base + i;
+                const double* qi = q + ((size_t)(base + i) * h_q + h) * d;
+                const double* doi = dout + ((size_t)(base + i) * h_q + h) * d;
+                const double pij = exp(scale * dot(qi, kj, d) - row_lse[ri]);
+                const double dzij = pij * (dot(doi, vj, d) - row_c[ri]);
+                for (int e = 0; e < d; ++e) {
+                    dkj[e] += scale * dzij * qi[e];
+                    dvj[e] += pij * doi[e];
+                }
+            }
+        }
+    }
+    /* dL/dS_h: sum of the rows' sink terms in token order */
     for (int h = 0; h < h_q; ++h) {
         double acc = 0.0;
-        for (int s = 0; s < nseq; ++s) acc += part[(size_t)s * h_q + h];
+        for (int t = 0; t < T; ++t) acc += row_sink[(size_t)h * T + t];
         dsinks[h] = acc;
     }
-    free(part);
+    free(ts);
+    free(row_lse);
+    free(row_c);
+    free(row_sink);
     return bad ? -1 : 0;
 }
 

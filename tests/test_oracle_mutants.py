@@ -20,18 +20,21 @@ MUTANTS = {
     "sink_multiplied_by_scale": ("z[n] = sinks[h];", "z[n] = P->scale * sinks[h];"),
     "sink_column_gets_upstream_gradient": ("u[n] = 0.0;", "u[n] = 1.0;"),
     "softmax_jacobian_sign": ("dz[t] = p[t] * (u[t] - c);", "dz[t] = p[t] * (c - u[t]);"),
-    "dv_uses_score_gradient": ("dvj[c] += p[t] * doi[c];", "dvj[c] += dz[t] * doi[c];"),
-    "dk_misses_scale": ("dkj[c] += gs * qi[c];", "dkj[c] += dz[t] * qi[c];"),
-    "dq_transposed_operand": ("dqi[c] += gs * kj[c];", "dqi[c] += gs * qi[c];"),
+    "dv_uses_score_gradient": ("dvj[e] += pij * doi[e];", "dvj[e] += dzij * doi[e];"),
+    "dk_misses_scale": ("dkj[e] += scale * dzij * qi[e];", "dkj[e] += dzij * qi[e];"),
+    "dq_uses_values_not_keys": ("const double* kj = k + ((size_t)(base + j0 + m) * h_kv + hk) * d;",
+                                "const double* kj = v + ((size_t)(base + j0 + m) * h_kv + hk) * d;"),
+    "key_pass_drops_row_term_c": ("(dot(doi, vj, d) - row_c[ri])", "(dot(doi, vj, d))"),
+    "key_pass_mask_off_by_one": ("if (j < j0 || j >= j1) continue;", "if (j < j0 || j > j1) continue;"),
     "window_off_by_one": ("i - P->window + 1 > 0) *j0 = i - P->window + 1;",
                           "i - P->window > 0) *j0 = i - P->window;"),
     "causal_excludes_diagonal": ("*j1 = i + 1;", "*j1 = i + (i > 0 ? 0 : 1);"),
     "gqa_wrong_kv_head": ("const int g = P->h_q / P->h_kv, hk = h / g, d = P->d;\n    const int n = j1 - j0;\n    const double* qi",
                           "const int g = P->h_q / P->h_kv, hk = h % P->h_kv, d = P->d;\n    const int n = j1 - j0;\n    const double* qi"),
     "lse_without_max": ("return m + log(sum);", "return log(sum);"),
-    "dsink_sign": ("dsink += dz[n];", "dsink -= dz[n];"),
-    "output_includes_sink_value": ("for (int t = 0; t < j1 - j0; ++t) {\n                        const double* vj",
-                                   "for (int t = 0; t <= j1 - j0 && t < L - j0; ++t) {\n                        const double* vj"),
+    "dsink_sign": ("row_sink[(size_t)h * T + t] = dz[n];", "row_sink[(size_t)h * T + t] = -dz[n];"),
+    "output_includes_sink_value": ("for (int u = 0; u < j1 - j0; ++u) {",
+                                   "for (int u = 0; u <= j1 - j0 && u < L - j0; ++u) {"),
 }
 
 
