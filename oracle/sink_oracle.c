@@ -70,6 +70,15 @@ static void allowed_keys(const problem_t* P, int i, int L, int* j0, int* j1) {
     if (P->window > 0 && i - P->window + 1 > 0) *j0 = i - P->window + 1;
 }
 
+/* Rows that can see key j, the same mask read from the key's side:
+ * positions [*i0, *i1). Every row in the range is still checked against
+ * allowed_keys before it contributes. */
+static void rows_seeing(const problem_t* P, int j, int L, int* i0, int* i1) {
+    *i0 = P->causal ? j : 0;
+    *i1 = L;
+    if (P->causal && P->window > 0 && j + P->window < L) *i1 = j + P->window;
+}
+
 static double dot(const double* a, const double* b, int d) {
     double s = 0.0;
     for (int c = 0; c < d; ++c) s += a[c] * b[c];
@@ -272,8 +281,10 @@ int sink_oracle_backward(int nseq, const int32_t* cu_seqlens, int h_q, int h_kv,
         double* dkj = dk + kv_off;
         double* dvj = dv + kv_off;
         for (int e = 0; e < d; ++e) dkj[e] = dvj[e] = 0.0;
+        int i0, i1;
+        rows_seeing(&P, j, L, &i0, &i1);
         for (int h = hk * g; h < (hk + 1) * g; ++h) {
-            for (int i = 0; i < L; ++i) {
+            for (int i = i0; i < i1; ++i) {
                 if (i < row_begin || i >= row_end) continue;
                 int j0, j1;
                 allowed_keys(&P, i, L, &j0, &j1);

@@ -25,12 +25,14 @@ MUTANTS = {
     "dq_uses_values_not_keys": ("const double* kj = k + ((size_t)(base + j0 + m) * h_kv + hk) * d;",
                                 "const double* kj = v + ((size_t)(base + j0 + m) * h_kv + hk) * d;"),
     "key_pass_drops_row_term_c": ("(dot(doi, vj, d) - row_c[ri])", "(dot(doi, vj, d))"),
-    "key_pass_mask_off_by_one": ("if (j < j0 || j >= j1) continue;", "if (j < j0 || j > j1) continue;"),
+    "key_pass_skips_diagonal": ("*i0 = P->causal ? j : 0;", "*i0 = P->causal ? j + 1 : 0;"),
     "window_off_by_one": ("i - P->window + 1 > 0) *j0 = i - P->window + 1;",
                           "i - P->window > 0) *j0 = i - P->window;"),
     "causal_excludes_diagonal": ("*j1 = i + 1;", "*j1 = i + (i > 0 ? 0 : 1);"),
     "gqa_wrong_kv_head": ("const int g = P->h_q / P->h_kv, hk = h / g, d = P->d;\n    const int n = j1 - j0;\n    const double* qi",
                           "const int g = P->h_q / P->h_kv, hk = h % P->h_kv, d = P->d;\n    const int n = j1 - j0;\n    const double* qi"),
+    "key_pass_window_too_short": ("if (P->causal && P->window > 0 && j + P->window < L) *i1 = j + P->window;",
+                                  "if (P->causal && P->window > 0 && j + P->window - 1 < L) *i1 = j + P->window - 1;"),
     "lse_without_max": ("return m + log(sum);", "return log(sum);"),
     "dsink_sign": ("row_sink[(size_t)h * T + t] = dz[n];", "row_sink[(size_t)h * T + t] = -dz[n];"),
     "output_includes_sink_value": ("for (int u = 0; u < j1 - j0; ++u) {",
