@@ -1,0 +1,87 @@
+// common.cuh - problem descriptor and small device helpers shared by the
+// kernels of libsinkattn (sink attention for sm_103a).
+//
+// Masks follow the C ABI in include/sink_attn.h: per sequence, positions are
+// counted from the sequence start; row i sees keys [lo(i), hi(i)) with
+//   causal = 0: [0, L)        causal = 1: [0, i+1)       window W: [max(0, i-W+1), i+1).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sinkattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device flag bits written into the first word of the workspace.
+constexpr uint32_t kFlagTimeout = 1u << 0;    // a bounded wait gave up
+constexpr uint32_t kFlagSeqTooLong = 1u << 1;  // a sequence longer than max_seqlen
+
+struct Problem {
+    int nseq;          // number of sequences
+    int max_seqlen;    // grid bound on a sequence's length
+    int total;         // T
+    int h_q, h_kv, group;  // group = h_q / h_kv
+    int head_dim;
+    int causal, window;
+    float scale;       // softmax scale on Q.K
+    float scale_log2;  // scale * log2(e): scores in base-2 units
+    const int32_t* cu; // device cu_seqlens or nullptr (padded: sequence s = [s*N, s*N+N))
+};
+
+__device__ __forceinline__ void seq_bounds(const Problem& P, int s, int& start, int& len) {
+    if (P.cu) {
+        start = __ldg(P.cu + s);
+        len = __ldg(P.cu + s + 1) - start;
+    } else {
+        start = s * P.max_seqlen;
+        len = P.max_seqlen;
+    }
+}
+
+// First allowed key of row i.
+__device__ __forceinline__ int key_lo(const Problem& P, int i) {
+    if (!P.causal) return 0;
+    if (P.window > 0) return i - P.window + 1 > 0 ? i - P.window + 1 : 0;
+    return 0;
+}
+
+// One past the last allowed key of row i in a sequence of length L.
+__device__ __forceinline__ int key_hi(const Problem& P, int i, int L) {
+    return P.causal ? i + 1 : L;
+}
+
+// One past the last row that sees key j (sequence length L).
+__device__ __forceinline__ int row_hi(const Problem& P, int j, int L) {
+    if (P.causal && P.window > 0) return j + P.window < L ? j + P.window : L;
+    return L;
+}
+
+// First row that sees key j.
+__device__ __forceinline__ int row_lo(const Problem& P, int j) {
+    return P.causal ? j : 0;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace sinkattn

@@ -1,0 +1,28 @@
+// kernels.h - internal launchers of libsinkattn (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sinkattn {
+
+// Counts every kernel launch the library enqueues (sink_attn_kernel_launches).
+void count_launches(unsigned n);
+
+// CUDA-core path (any dtype the ABI accepts, head_dim 64).
+cudaError_t simt_fwd(const Problem& P, bool bf16, const void* q, const void* k, const void* v,
+                     const float* sinks, void* o, float* lse, uint32_t* flags, cudaStream_t st);
+cudaError_t simt_bwd_main(const Problem& P, bool bf16, const void* q, const void* k, const void* v,
+                          const float* lse, const float* delta, const void* dout, void* dq,
+                          void* dk, void* dv, cudaStream_t st);
+
+// Backward step 1 (memory-bound): delta [h_q, T] and dsinks [h_q] via
+// per-chunk partials [h_q, preprocess_chunks(T)] reduced in a fixed order.
+int preprocess_chunks(int total);
+cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, const void* o,
+                           const float* lse, const void* dout, float* delta, float* dsinks,
+                           float* partial, cudaStream_t st);
+
+}  // namespace sinkattn

@@ -1,0 +1,23 @@
+// tc.h - tensor-core (tcgen05 / TMEM / TMA) path of libsinkattn for sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sinkattn {
+
+bool tc_fwd_supported(const Problem& P, bool bf16);
+size_t tc_fwd_workspace_bytes(const Problem& P, bool bf16);
+cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
+                   const float* sinks, void* o, float* lse, uint32_t* flags, void* workspace,
+                   cudaStream_t st);
+
+bool tc_bwd_supported(const Problem& P, bool bf16);
+size_t tc_bwd_workspace_bytes(const Problem& P, bool bf16);
+cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v,
+                   const float* lse, const float* delta, const void* dout, void* dq, void* dk,
+                   void* dv, uint32_t* flags, void* workspace, cudaStream_t st);
+
+}  // namespace sinkattn

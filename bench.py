@@ -1,0 +1,399 @@
+"""Benchmark: sink-attention forward + backward (incl. dS_h) on GB300.
+
+One step = one pass of the whole hot path over one batch: sink_attn_fwd, then
+sink_attn_bwd_preprocess (delta and dS_h) and sink_attn_bwd_main (dQ, dK, dV),
+all through the C ABI. The default workload is the GPT-OSS-20B-shaped
+full-causal layer (B=2, N=8192, H_q=64, H_kv=8, d=64, bf16). Its inputs (302 MB
+of Q/K/V/dO) exceed the 129 MB L2, so no extra flush is done between steps.
+
+FLOP convention (algorithmic, unmasked (row, key) pairs only): forward 4*d per
+pair (QK^T and PV), backward 10*d per pair (QK^T recompute, dP, dV, dK, dQ).
+
+Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
+instead (the only reference this method has), on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_sink_softmax_gb300 import inputs  # noqa: E402
+
+METRIC = "sink-attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- workload math
+def pairs_of(w: inputs.Workload, window: int) -> int:
+    """Number of unmasked (row, key) pairs summed over heads and sequences."""
+    lengths = w.lengths if w.packed else [w.seqlen] * w.batch
+    total = 0
+    for L in lengths:
+        if not w.causal:
+            n = L * L
+        elif window and window > 0:
+            W = window
+            full = max(L - W + 1, 0)  # rows i >= W-1 see W keys
+            head = min(L, W - 1)      # rows i < W-1 see i+1 keys
+            n = head * (head + 1) // 2 + full * W
+        else:
+            n = L * (L + 1) // 2
+        total += n
+    return total * w.h_q
+
+
+def flops_of(w, window):
+    p = pairs_of(w, window)
+    return 4 * w.head_dim * p, 10 * w.head_dim * p
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_source, stage):
+    """DRAM traffic per launch from the committed ncu summary, if the kernel's
+    source is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(kernel_source)
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            if line.startswith("| ") and f"| {stage} |" in line:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                # | stage | source digest | bytes per launch | ...
+                if len(cells) >= 3 and cells[1] == digest:
+                    try:
+                        return float(cells[2])
+                    except ValueError:
+                        return None
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def time_oracle(w, prob, window, budget_s=20.0, heads=None):
+    """fp64 oracle fwd+bwd on a bounded sample: batch/sequence 0, the query heads
+    of key/value head 0 (or ``heads`` of them), all rows. Returns a dict."""
+    import oracle
+    g = w.h_q // w.h_kv
+    nh = heads or g
+    if w.packed:
+        cu = prob["cu_seqlens"]
+        a, e = int(cu[0]), int(cu[1])
+        q, k, v, do = (prob[n][a:e] for n in ("q", "k", "v", "dout"))
+        L = e - a
+    else:
+        q, k, v, do = (prob[n][0] for n in ("q", "k", "v", "dout"))
+        L = w.seqlen
+    q, do = q[:, :nh], do[:, :nh]
+    k, v = k[:, :1], v[:, :1]
+    s = prob["sinks"][:nh]
+    kw = dict(scale=w.scale if w.scale else 1 / math.sqrt(w.head_dim), causal=w.causal, window=window)
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, s, **kw)
+    oracle.backward(q, k, v, s, do, **kw)
+    dt = time.perf_counter() - t0
+    sw = inputs.Workload("sample", 1, L, nh, 1, w.head_dim, w.dtype, w.causal, window, 0)
+    f_fwd, f_bwd = flops_of(sw, window)
+    return {"seconds": dt, "flops": f_fwd + f_bwd, "cores": oracle.num_threads(),
+            "sample": f"sequence 0 (length {L}), query heads 0..{nh - 1} of key/value head 0, "
+                      f"all rows, fp64 forward + backward",
+            "value": (f_fwd + f_bwd) / dt / 1e12}
+
+
+def run_reference(args, w, window):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    prob = inputs.make_inputs(w)
+    for _ in range(args.warmup):
+        time_oracle(w, prob, window, heads=1)
+    times, flops, info = [], 0, None
+    for _ in range(args.steps):
+        info = time_oracle(w, prob, window, heads=1)
+        times.append(info["seconds"])
+        flops = info["flops"]
+    ms = 1000 * sum(times) / len(times)
+    value = flops / (ms / 1000) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample": info["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"],
+                         "kind": "oracle", "sample": info["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, w, window):
+    import attention_sink_softmax_gb300 as sa
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    prob_host = inputs.make_inputs(w, seed=w.seed + rank)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in prob_host.items()}
+    q, k, v, sinks, dout, cu = d["q"], d["k"], d["v"], d["sinks"], d["dout"], d["cu_seqlens"]
+    p = sa.make_params(q, k, cu, max_seqlen=w.seqlen, causal=w.causal, window=window,
+                       softmax_scale=w.scale)
+    o = torch.empty_like(q)
+    lse = torch.empty(p.h_q, p.total_tokens, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsinks = torch.empty_like(sinks)
+    delta = torch.empty(p.h_q, p.total_tokens, dtype=torch.float32, device=dev)
+    wsz = max(sa.sink_attn_workspace_bytes(p, False), sa.sink_attn_workspace_bytes(p, True))
+    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
+        if ev is not None:
+            ev[1].record(stream)
+        sa.sink_attn_bwd_preprocess(p, sinks, o, lse, dout, delta=delta, dsinks=dsinks,
+                                    workspace=work)
+        if ev is not None:
+            ev[2].record(stream)
+        sa.sink_attn_bwd_main(p, q, k, v, lse, delta, dout, cu, dq=dq, dk=dk, dv=dv,
+                              workspace=work)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, flags = sa.sink_attn_fetch_device_error(work)
+    if st != 0:
+        raise RuntimeError(f"device flagged an error during warm-up: status {st}, flags {flags}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = sa.sink_attn_kernel_launches()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(ws)
+    launches = sa.sink_attn_kernel_launches() - launches0
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, ws, dev)
+    stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
+    st, flags = sa.sink_attn_fetch_device_error(work)
+    if st != 0:
+        raise RuntimeError(f"device flagged an error: status {st}, flags {flags}")
+
+    f_fwd, f_bwd = flops_of(w, window)
+    flops_step = f_fwd + f_bwd
+    value = flops_step * ws / (ms / 1000) / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned)
+    host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv),
+                             ("dsinks", dsinks))}
+    dev_in = {"q": q, "k": k, "v": v, "sinks": sinks, "dout": dout}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
+        sa.sink_attn_bwd(q, k, v, sinks, o, lse, dout, cu, dq=dq, dk=dk, dv=dv, dsinks=dsinks,
+                         workspace=work, params=p)
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dsinks", dsinks)):
+            host_out[n].copy_(t, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    e2e_value = flops_step * ws / (ms_e2e / 1000) / 1e12
+
+    pk, pk_src = peaks()
+    # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop
+    main_ms = stage_ms[2]
+    main_tflops = f_bwd / (main_ms / 1000) / 1e12
+    csrc = os.path.join(ROOT, "attention_sink_softmax_gb300", "csrc")
+    main_src = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
+                      if f.endswith((".cu", ".cuh", ".h")))
+    traffic = profiled_traffic(main_src, "bwd_main")
+    roofline = {"bound": "tensor", "achieved": main_tflops,
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
+                "kernel": "sink_attn_bwd_main", "peak_kind": f"bf16 sustained ({pk_src})"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen, "h_q": w.h_q,
+                   "h_kv": w.h_kv, "head_dim": w.head_dim, "causal": w.causal,
+                   "window": window, "tokens": w.total_tokens,
+                   "flops_per_step": flops_step, "l2": "inputs exceed L2 (no flush)",
+                   "parallelism": f"replicas x{ws} (independent batches, no collective)"},
+        "pct_of_peak": {"burst": 100 * value / ws / pk["bf16_tflops"],
+                        "sustained": 100 * value / ws / pk["bf16_tflops_sustained"],
+                        "source": pk_src},
+        "stages_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1], "bwd_main": stage_ms[2]},
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        info = time_oracle(w, prob_host, window)
+        line["cpu_baseline"] = {"value": info["value"], "unit": "TFLOP/s", "cores": info["cores"],
+                                "kind": "oracle", "sample": info["sample"],
+                                "seconds": info["seconds"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=1, help="workload index 0..4")
+    ap.add_argument("--window", type=int, default=None, help="override the workload's window")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = inputs.workload(args.config)
+    window = w.window if args.window is None else args.window
+    if args.impl == "reference":
+        run_reference(args, w, window)
+    else:
+        run_gpu(args, w, window)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * sink_attn.h - C ABI of libsinkattn: forward and backward of causal /
+ * sliding-window grouped-query attention with one learnable sink logit per
+ * query head, for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed. The operation is the one defined on the page
+ * "惊爆！GPT-OSS-20B强化学习，训练速度狂飙、超稳定！" (nmedialink.com):
+ *   - section "GPT-OSS中的带注意力槽的注意力机制": the scaled scores of a row are
+ *     concatenated with the head's sink logit, softmax runs over the N_k + 1
+ *     columns, the sink column is dropped, and the remaining probabilities
+ *     multiply V;
+ *   - section "数学公式深入解读": P_ij = exp(S_ij) / (sum_j' exp(S_ij') + exp(S_h))
+ *     with S_ij = scale * Q_i . K_j, and the sink probability
+ *     P_{i,h} = exp(S_h) / (same denominator);
+ *   - section "反向传播的实现": dL/dS_h = -sum_i P_{i,h} sum_j P_ij dL/dP_ij,
+ *     which equals -sum_i P_{i,h} * (dO_i . O_i) because the sink column has
+ *     no upstream gradient.
+ * Readings where the page is silent: the sink is a raw logit (not multiplied
+ * by the scale); there is one sink per query head; a window W means keys
+ * i-W+1 .. i and is always causal; packed sequences are masked independently,
+ * with positions counted from each sequence's start.
+ *
+ * Per row i of query head h (key/value head h / (h_q / h_kv)):
+ *   A(i)   = allowed keys: all keys of the sequence (causal = 0), keys 0..i
+ *            (causal = 1, window <= 0) or keys max(0, i-W+1)..i (window = W);
+ *   M_i    = max(S_h, max_{j in A(i)} S_ij)
+ *   LSE_i  = M_i + ln(exp(S_h - M_i) + sum_{j in A(i)} exp(S_ij - M_i))
+ *   O_i    = sum_{j in A(i)} exp(S_ij - LSE_i) V_j
+ *
+ * Layouts (row-major, contiguous, device memory):
+ *   padded (cu_seqlens == NULL): q/o/dout/dq [B, N, h_q, d], k/v/dk/dv [B, N, h_kv, d]
+ *   packed (cu_seqlens != NULL): q/o/dout/dq [T, h_q, d],     k/v/dk/dv [T, h_kv, d]
+ *   sinks, dsinks: [h_q] fp32.  lse: [h_q, T] fp32 (T = B * N when padded).
+ *   cu_seqlens: int32 [batch + 1], device memory, cu_seqlens[0] = 0,
+ *   non-decreasing, cu_seqlens[batch] = total_tokens.
+ * Every pointer must be 16-byte aligned (cu_seqlens: 4-byte). q/k/v/o/dout/dq/dk/dv use the dtype
+ * given in the params; sinks, dsinks and lse are always fp32.
+ *
+ * Ownership and execution. The caller allocates every buffer, including the
+ * workspace (size from sink_attn_workspace_bytes). No entry point allocates,
+ * frees or synchronises except sink_attn_fetch_device_error, which says so.
+ * Work is enqueued on the caller's stream; outputs are valid once that stream
+ * reaches the enqueued work. Outputs (o, lse, dq, dk, dv, dsinks) are
+ * overwritten, never accumulated into. Inputs are not modified.
+ *
+ * Errors. Every entry point returns a status. Arguments are validated before
+ * anything is enqueued; an invalid call enqueues nothing. A failed launch is
+ * reported as SINK_ERR_CUDA. Conditions found on the device (a wait that gave
+ * up, a sequence longer than max_seqlen) set a flag word at the start of the
+ * workspace; sink_attn_fetch_device_error reads and clears it. Nothing is
+ * thrown across the ABI.
+ */
+#ifndef SINK_ATTN_H
+#define SINK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SINK_API __attribute__((visibility("default")))
+#else
+#define SINK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sink_stream_t; /* same object as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    SINK_OK = 0,
+    SINK_ERR_INVALID_ARG = 1,  /* a NULL/misaligned pointer, a bad size or an inconsistent field */
+    SINK_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim != 64) */
+    SINK_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    SINK_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than sink_attn_workspace_bytes */
+    SINK_ERR_TIMEOUT = 5,      /* a kernel's bounded wait gave up (reported by fetch_device_error) */
+    SINK_ERR_DEVICE = 6        /* another condition flagged on the device (see fetch_device_error) */
+} sink_status_t;
+
+typedef enum { SINK_BF16 = 0, SINK_FP32 = 1 } sink_dtype_t;
+
+typedef struct {
+    int batch;            /* number of sequences: B (padded) or the length of cu_seqlens minus 1 */
+    int max_seqlen;       /* N (padded) or an upper bound on every packed sequence's length */
+    int total_tokens;     /* T: B * N (padded) or cu_seqlens[batch] (packed) */
+    int h_q;              /* query heads; a multiple of h_kv */
+    int h_kv;             /* key/value heads */
+    int head_dim;         /* d; 64 is supported */
+    sink_dtype_t dtype;   /* dtype of q, k, v, o, dout, dq, dk, dv */
+    float softmax_scale;  /* scale applied to Q.K; <= 0 selects 1/sqrt(head_dim) */
+    int causal;           /* 1: causal mask; 0: every key of the sequence (window must be 0) */
+    int window;           /* <= 0: no window; W > 0: keys i-W+1 .. i (requires causal = 1) */
+} sink_attn_params_t;
+
+/* Bytes of device workspace that sink_attn_fwd (is_bwd = 0) or sink_attn_bwd /
+ * sink_attn_bwd_preprocess / sink_attn_bwd_main (is_bwd = 1) need for these
+ * params. Returns 0 if the params are invalid. The workspace needs no
+ * initialisation and may be reused across calls on the same stream. */
+SINK_API size_t sink_attn_workspace_bytes(const sink_attn_params_t* params, int is_bwd);
+
+/* Forward (sections "GPT-OSS中的带注意力槽的注意力机制" and "数学公式深入解读"):
+ * writes o (input dtype) and lse (fp32 [h_q, T], natural log, sink included). */
+SINK_API sink_status_t sink_attn_fwd(const sink_attn_params_t* params,
+                            const void* q, const void* k, const void* v,
+                            const float* sinks, const int32_t* cu_seqlens,
+                            void* o, float* lse,
+                            void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
+/* Full backward (section "反向传播的实现"): given the forward's o and lse and the
+ * upstream gradient dout, writes dq (input dtype), dk, dv (input dtype, summed
+ * over the query heads of each key/value head) and dsinks (fp32 [h_q],
+ * dL/dS_h summed over every sequence and row of head h, reduced in a fixed
+ * order so it is bitwise reproducible). Equivalent to sink_attn_bwd_preprocess
+ * into workspace followed by sink_attn_bwd_main. */
+SINK_API sink_status_t sink_attn_bwd(const sink_attn_params_t* params,
+                            const void* q, const void* k, const void* v,
+                            const float* sinks, const int32_t* cu_seqlens,
+                            const void* o, const float* lse, const void* dout,
+                            void* dq, void* dk, void* dv, float* dsinks,
+                            void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
+/* Backward step 1 (section "反向传播的实现", simplified equation): writes
+ * delta[h, t] = dout_t,h . o_t,h (fp32 [h_q, T]) and
+ * dsinks[h] = -sum_t exp(S_h - lse[h, t]) * delta[h, t]. Memory-bound. */
+SINK_API sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params,
+                                       const float* sinks, const void* o, const float* lse,
+                                       const void* dout, float* delta, float* dsinks,
+                                       void* workspace, size_t workspace_bytes,
+                                       sink_stream_t stream);
+
+/* Backward step 2: recomputes P = exp(S - lse) and writes dq, dk, dv, using
+ * delta from step 1. dS_ij = P_ij (dout_i . v_j - delta_i). */
+SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
+                                 const void* q, const void* k, const void* v,
+                                 const int32_t* cu_seqlens, const float* lse,
+                                 const float* delta, const void* dout,
+                                 void* dq, void* dk, void* dv,
+                                 void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
+/* Reads and clears the device flag word at the start of a workspace that was
+ * passed to the calls above. SYNCHRONISES the stream (it copies 4 bytes back).
+ * Returns SINK_OK, SINK_ERR_TIMEOUT (a bounded wait gave up: outputs of that
+ * call are invalid), SINK_ERR_DEVICE (a sequence exceeded max_seqlen: rows past
+ * it were not computed) or SINK_ERR_CUDA. *flags_out (may be NULL) receives the
+ * raw flag bits. */
+SINK_API sink_status_t sink_attn_fetch_device_error(void* workspace, size_t workspace_bytes,
+                                           sink_stream_t stream, uint32_t* flags_out);
+
+/* Static description of a status code. Never NULL. */
+SINK_API const char* sink_attn_status_str(sink_status_t status);
+
+/* Number of kernels this library has enqueued in the calling process so far
+ * (all entry points, all devices). Host-side counter; never synchronises. */
+SINK_API uint64_t sink_attn_kernel_launches(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+SINK_API int sink_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SINK_ATTN_H */

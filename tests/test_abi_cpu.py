@@ -1,0 +1,111 @@
+"""Host-side checks of libsinkattn that need no GPU: the library loads, exports
+every entry point include/*.h declares, and rejects invalid arguments before
+touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import attention_sink_softmax_gb300 as sa
+from attention_sink_softmax_gb300 import _abi
+from attention_sink_softmax_gb300 import build as sa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    sa_build.build()
+    return _abi.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"SINK_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert set(_abi.EXPORTS) <= set(declared)
+    assert len(declared) >= 8
+    for name in declared:
+        assert hasattr(L, name), f"libsinkattn does not export {name}"
+
+
+def test_status_strings_and_version(L):
+    assert sa.sink_attn_status_str(0) == "ok"
+    for st in range(7):
+        assert isinstance(sa.sink_attn_status_str(st), str)
+    assert sa.sink_attn_status_str(99) == "unknown status"
+    assert sa.sink_attn_version() >= 100
+
+
+def _params(**kw):
+    p = _abi.SinkAttnParams()
+    base = dict(batch=2, max_seqlen=8192, total_tokens=16384, h_q=64, h_kv=8, head_dim=64,
+                dtype=_abi.SINK_BF16, softmax_scale=0.125, causal=1, window=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_workspace_sizes(L):
+    p = _params()
+    fwd = sa.sink_attn_workspace_bytes(p, False)
+    bwd = sa.sink_attn_workspace_bytes(p, True)
+    assert fwd >= 256 and fwd % 256 == 0
+    # the backward holds at least delta [h_q, T] fp32
+    assert bwd >= 256 + 4 * 64 * 16384
+    assert sa.sink_attn_workspace_bytes(_params(h_q=63), True) == 0
+    assert sa.sink_attn_workspace_bytes(_params(head_dim=128), True) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(h_q=63), _abi.SINK_ERR_INVALID_ARG),          # h_q not a multiple of h_kv
+    (dict(causal=0, window=128), _abi.SINK_ERR_INVALID_ARG),
+    (dict(head_dim=128), _abi.SINK_ERR_UNSUPPORTED),
+    (dict(dtype=7), _abi.SINK_ERR_INVALID_ARG),
+    (dict(total_tokens=100), _abi.SINK_ERR_INVALID_ARG),  # padded: T != B * N
+    (dict(batch=-1), _abi.SINK_ERR_INVALID_ARG),
+    (dict(causal=2), _abi.SINK_ERR_INVALID_ARG),
+])
+def test_invalid_params_rejected_before_launch(L, kw, status):
+    p = _params(**kw)
+    nul = ctypes.c_void_p(0)
+    st = L.sink_attn_fwd(ctypes.byref(p), *([nul] * 7), nul, 0, nul)
+    assert st == status
+    st = L.sink_attn_bwd(ctypes.byref(p), *([nul] * 12), nul, 0, nul)
+    assert st == status
+
+
+def test_missing_workspace_rejected(L):
+    p = _params()
+    nul = ctypes.c_void_p(0)
+    assert L.sink_attn_fwd(ctypes.byref(p), *([nul] * 7), nul, 0, nul) == _abi.SINK_ERR_WORKSPACE
+    assert L.sink_attn_bwd(ctypes.byref(p), *([nul] * 12), nul, 0, nul) == _abi.SINK_ERR_WORKSPACE
+    assert L.sink_attn_fetch_device_error(nul, 0, nul, None) == _abi.SINK_ERR_WORKSPACE
+
+
+def test_host_memory_workspace_rejected(L):
+    """A host buffer is never handed to a kernel: the call fails up front."""
+    p = _params()
+    buf = ctypes.create_string_buffer(1 << 20)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    nul = ctypes.c_void_p(0)
+    st = L.sink_attn_fwd(ctypes.byref(p), *([nul] * 7), ctypes.c_void_p(addr), 1 << 19, nul)
+    assert st == _abi.SINK_ERR_WORKSPACE
+
+
+def test_python_layer_rejects_cpu_tensors(L):
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sa.sink_attn_fwd(q, k, k, torch.zeros(2))

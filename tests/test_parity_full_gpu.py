@@ -1,0 +1,191 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times (the same C-ABI calls on the full inputs).
+
+The GPU computes the whole problem; the oracle computes exact sub-problems it
+can finish in seconds, and the GPU outputs they cover are compared element by
+element:
+  - one (sequence, key/value head) unit: all its rows and keys (its query
+    heads' O, LSE, dQ; its dK, dV), since units are independent;
+  - under a causal mask, the first R rows of a sequence are the whole problem
+    of length R (O, LSE, dQ of those rows);
+  - rows [N-R, N) evaluated over all keys give O, LSE, dQ of those rows and
+    dK, dV of keys >= N-R exactly, since only those rows see those keys;
+  - dS_h = -sum over all rows of P_sink * (dO . O) from the oracle's O and LSE
+    (the page's simplified sink-gradient equation).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_sink_softmax_gb300 as sa
+import oracle
+from attention_sink_softmax_gb300 import inputs
+from parity import assert_close, d_rounding_allowances, dsink_allowance
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _gpu(w, prob, window):
+    d = {k: (v.to(DEV) if v is not None else None) for k, v in prob.items()}
+    o, lse = sa.sink_attn_fwd(d["q"], d["k"], d["v"], d["sinks"], d["cu_seqlens"],
+                              max_seqlen=w.seqlen, causal=w.causal, window=window,
+                              softmax_scale=w.scale)
+    dq, dk, dv, ds = sa.sink_attn_bwd(d["q"], d["k"], d["v"], d["sinks"], o, lse, d["dout"],
+                                      d["cu_seqlens"], max_seqlen=w.seqlen, causal=w.causal,
+                                      window=window, softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    out = [t.cpu() for t in (o, lse, dq, dk, dv, ds)]
+    del d, o, lse, dq, dk, dv, ds
+    torch.cuda.empty_cache()
+    return out
+
+
+def _sink_grad_from_forward(o, lse, dout, sinks_h):
+    """-sum_t exp(S_h - LSE_t) (dO_t . O_t) for one head; o, dout [T, d], lse [T]."""
+    D = np.einsum("td,td->t", np.asarray(dout, np.float64), o)
+    return -float(np.sum(np.exp(sinks_h - lse) * D))
+
+
+def _unit(prob, b, hk, g, padded):
+    """Tensors of sequence b restricted to key/value head hk and its query heads."""
+    hs = slice(hk * g, (hk + 1) * g)
+    if padded:
+        return (prob["q"][b, :, hs], prob["k"][b, :, hk:hk + 1], prob["v"][b, :, hk:hk + 1],
+                prob["sinks"][hs], prob["dout"][b, :, hs])
+    cu = prob["cu_seqlens"]
+    a, e = int(cu[b]), int(cu[b + 1])
+    return (prob["q"][a:e, hs], prob["k"][a:e, hk:hk + 1], prob["v"][a:e, hk:hk + 1],
+            prob["sinks"][hs], prob["dout"][a:e, hs])
+
+
+def _check_unit(w, got, prob, b, hk, window, report, tag, dsink_batches=()):
+    g = w.h_q // w.h_kv
+    padded = not w.packed
+    q, k, v, s, do = _unit(prob, b, hk, g, padded)
+    kw = dict(scale=w.scale, causal=w.causal, window=window)
+    o, lse = oracle.forward(q, k, v, s, **kw)
+    dq, dk, dv, ds = oracle.backward(q, k, v, s, do, **kw)
+    go, glse, gdq, gdk, gdv, gds = got
+    hs = slice(hk * g, (hk + 1) * g)
+    if padded:
+        N = w.seqlen
+        tsl = slice(b * N, (b + 1) * N)
+        sel = lambda t: t[b, :, hs]
+        selk = lambda t: t[b, :, hk:hk + 1]
+    else:
+        cu = prob["cu_seqlens"]
+        tsl = slice(int(cu[b]), int(cu[b + 1]))
+        sel = lambda t: t[tsl, hs]
+        selk = lambda t: t[tsl, hk:hk + 1]
+    assert_close(f"{tag} O", sel(go), o, w.dtype, report)
+    assert_close(f"{tag} LSE", glse[hs, tsl], lse, w.dtype, report, rounds_output=False)
+    assert_close(f"{tag} dQ", sel(gdq), dq, w.dtype, report)
+    assert_close(f"{tag} dK", selk(gdk), dk, w.dtype, report)
+    assert_close(f"{tag} dV", selk(gdv), dv, w.dtype, report)
+    if dsink_batches is not None:
+        total = ds.copy()
+        allow = dsink_allowance(o, lse, do, s, w.dtype)
+        for b2 in dsink_batches:
+            q2, k2, v2, s2, do2 = _unit(prob, b2, hk, g, padded)
+            o2, lse2 = oracle.forward(q2, k2, v2, s2, **kw)
+            for hh in range(g):
+                total[hh] += _sink_grad_from_forward(o2[:, hh], lse2[hh], do2[:, hh].to(torch.float64), float(s2[hh]))
+            allow = allow + dsink_allowance(o2, lse2, do2, s2, w.dtype)
+        assert_close(f"{tag} dS_h", gds[hs], total, w.dtype, report, allowance=allow,
+                     rounds_output=False)
+
+
+def test_full_causal_B2_N8192():
+    w = inputs.workload(1)
+    prob = inputs.make_inputs(w)
+    got = _gpu(w, prob, w.window)
+    rep = {}
+    _check_unit(w, got, prob, b=1, hk=5, window=0, report=rep, tag="cfg1 b1 hk5", dsink_batches=[0])
+    print(rep)
+
+
+def test_sliding_window_B4_N8192():
+    w = inputs.workload(2)
+    prob = inputs.make_inputs(w)
+    got = _gpu(w, prob, w.window)
+    rep = {}
+    _check_unit(w, got, prob, b=2, hk=1, window=128, report=rep, tag="cfg2 b2 hk1",
+                dsink_batches=[0, 1, 3])
+    _check_unit(w, got, prob, b=0, hk=6, window=128, report=rep, tag="cfg2 b0 hk6", dsink_batches=None)
+    print(rep)
+
+
+def test_packed_variable_length_both_layers():
+    w = inputs.workload(3)
+    prob = inputs.make_inputs(w)
+    lengths = np.array(w.lengths)
+    picks = [int(np.argmin(lengths)), int(np.argsort(lengths)[len(lengths) // 2]), int(np.argmax(lengths))]
+    rep = {}
+    for window in w.windows:
+        got = _gpu(w, prob, window)
+        for s in picks:
+            _check_unit(w, got, prob, b=s, hk=7, window=window, report=rep,
+                        tag=f"cfg3 win{window} seq{s} len{lengths[s]}", dsink_batches=None)
+        if window > 0:
+            # dS_h of query head 0 summed over all 48 sequences
+            g = w.h_q // w.h_kv
+            cu = prob["cu_seqlens"].numpy()
+            o, lse = oracle.forward(prob["q"][:, 0:1], prob["k"][:, 0:1], prob["v"][:, 0:1],
+                                    prob["sinks"][0:1], scale=w.scale, window=window,
+                                    cu_seqlens=cu)
+            exp = _sink_grad_from_forward(o[:, 0], lse[0], prob["dout"][:, 0].to(torch.float64),
+                                          float(prob["sinks"][0]))
+            allow = dsink_allowance(o, lse, prob["dout"][:, 0:1], prob["sinks"][0:1], w.dtype)
+            assert_close("cfg3 dS_h head0", got[5][0:1], np.array([exp]), w.dtype, rep,
+                         allowance=allow, rounds_output=False)
+    print(rep)
+
+
+def test_long_context_N32768_prefix_and_suffix():
+    w = inputs.workload(4)
+    prob = inputs.make_inputs(w)
+    got = _gpu(w, prob, 0)
+    go, glse, gdq, gdk, gdv, gds = got
+    rep = {}
+    g = w.h_q // w.h_kv
+    N = w.seqlen
+    kw = dict(scale=w.scale, causal=True, window=0)
+    for hk in (0, 7):
+        hs = slice(hk * g, (hk + 1) * g)
+        q, k, v, s, do = _unit(prob, 0, hk, g, True)
+        # prefix rows [0, R): the causal prefix is the whole problem of length R
+        R = 1024
+        o, lse = oracle.forward(q[:R], k[:R], v[:R], s, **kw)
+        dq, _, _, _ = oracle.backward(q[:R], k[:R], v[:R], s, do[:R], **kw)
+        adq, _ = d_rounding_allowances(q[:R], k[:R], v[:R], s, do[:R], o, dtype=w.dtype, **kw)
+        assert_close(f"cfg4 hk{hk} O prefix", go[0, :R, hs], o, w.dtype, rep)
+        assert_close(f"cfg4 hk{hk} LSE prefix", glse[hs, :R], lse, w.dtype, rep, rounds_output=False)
+        assert_close(f"cfg4 hk{hk} dQ prefix", gdq[0, :R, hs], dq, w.dtype, rep, allowance=adq)
+        # suffix rows [N-R2, N) over all keys
+        R2 = 384
+        o, lse = oracle.forward(q, k, v, s, row_begin=N - R2, **kw)
+        dq, dk, dv, _ = oracle.backward(q, k, v, s, do, row_begin=N - R2, **kw)
+        adq, adk = d_rounding_allowances(q, k, v, s, do, o, dtype=w.dtype, row_begin=N - R2, **kw)
+        assert_close(f"cfg4 hk{hk} O suffix", go[0, N - R2:, hs], o[N - R2:], w.dtype, rep)
+        assert_close(f"cfg4 hk{hk} LSE suffix", glse[hs, N - R2:], lse[:, N - R2:], w.dtype, rep,
+                     rounds_output=False)
+        assert_close(f"cfg4 hk{hk} dQ suffix", gdq[0, N - R2:, hs], dq[N - R2:], w.dtype, rep,
+                     allowance=adq[N - R2:])
+        assert_close(f"cfg4 hk{hk} dK suffix", gdk[0, N - R2:, hk:hk + 1], dk[N - R2:], w.dtype, rep,
+                     allowance=adk[N - R2:])
+        assert_close(f"cfg4 hk{hk} dV suffix", gdv[0, N - R2:, hk:hk + 1], dv[N - R2:], w.dtype, rep)
+    # dS_h of two heads (a large-sink and a small-sink one) over all rows
+    for h in (int(torch.argmax(prob["sinks"])), int(torch.argmin(prob["sinks"]))):
+        hk = h // g
+        o, lse = oracle.forward(prob["q"][0, :, h:h + 1], prob["k"][0, :, hk:hk + 1],
+                                prob["v"][0, :, hk:hk + 1], prob["sinks"][h:h + 1], **kw)
+        exp = _sink_grad_from_forward(o[:, 0], lse[0], prob["dout"][0, :, h].to(torch.float64),
+                                      float(prob["sinks"][h]))
+        allow = dsink_allowance(o, lse, prob["dout"][0, :, h:h + 1], prob["sinks"][h:h + 1], w.dtype)
+        assert_close(f"cfg4 dS_h head{h}", gds[h:h + 1], np.array([exp]), w.dtype, rep,
+                     allowance=allow, rounds_output=False)
+    print(rep)

@@ -1,0 +1,181 @@
+"""GPU parity of libsinkattn against the fp64 oracle, element by element, on
+seeded inputs that span several tiles with ragged tails, plus edge cases.
+
+All calls go through the C ABI (via the ctypes binding)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_sink_softmax_gb300 as sa
+from attention_sink_softmax_gb300 import _abi, inputs
+from parity import assert_close, assert_dsinks_close, d_rounding_allowances, oracle_fwd_bwd
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _run(prob, *, causal=True, window=0, scale=None, max_seqlen=None):
+    d = {k: (v.to(DEV) if v is not None else None) for k, v in prob.items()}
+    o, lse = sa.sink_attn_fwd(d["q"], d["k"], d["v"], d["sinks"], d["cu_seqlens"],
+                              max_seqlen=max_seqlen, causal=causal, window=window,
+                              softmax_scale=scale)
+    dq, dk, dv, ds = sa.sink_attn_bwd(d["q"], d["k"], d["v"], d["sinks"], o, lse, d["dout"],
+                                      d["cu_seqlens"], max_seqlen=max_seqlen, causal=causal,
+                                      window=window, softmax_scale=scale)
+    torch.cuda.synchronize()
+    return o, lse, dq, dk, dv, ds
+
+
+def _check(prob, dtype, *, causal=True, window=0, scale=None):
+    hd = prob["q"].shape[-1]
+    sc = scale if scale is not None else 1.0 / math.sqrt(hd)
+    got = _run(prob, causal=causal, window=window, scale=scale)
+    ref = oracle_fwd_bwd(prob["q"], prob["k"], prob["v"], prob["sinks"], prob["dout"], scale=sc,
+                         causal=causal, window=window, cu_seqlens=prob["cu_seqlens"])
+    adq, adk = d_rounding_allowances(prob["q"], prob["k"], prob["v"], prob["sinks"], prob["dout"],
+                                     ref[0], scale=sc, causal=causal, window=window, dtype=dtype,
+                                     cu_seqlens=prob["cu_seqlens"])
+    allow = {"dQ": adq, "dK": adk}
+    for name, g, r in zip(("O", "LSE", "dQ", "dK", "dV"), got[:5], ref[:5]):
+        a = allow.get(name)
+        assert_close(name, g, r.reshape(tuple(g.shape)), dtype, rounds_output=(name != "LSE"),
+                     allowance=None if a is None else a.reshape(tuple(g.shape)))
+    T, H = ref[1].shape[1], ref[1].shape[0]
+    assert_dsinks_close("dS_h", got[5], ref[5], dtype, ref[0].reshape(T, H, hd), ref[1],
+                        prob["dout"].reshape(T, H, hd), prob["sinks"])
+    return got
+
+
+def test_tiny_fp32_workload_full_oracle():
+    """B=1, N=128, H_q=4, H_kv=1, d=64, fp32, causal, seed 0: every output."""
+    w = inputs.workload(0)
+    prob = inputs.make_inputs(w)
+    _check(prob, torch.float32)
+
+
+CASES = [
+    # lengths, h_q, h_kv, packed, causal, window
+    ([300, 300], 8, 2, False, True, 0),        # padded, 3 tiles + ragged tail
+    ([1, 127, 129, 255, 300], 4, 1, True, True, 0),
+    ([517], 8, 8, True, True, 128),            # MHA, window 128
+    ([640, 33], 8, 1, True, True, 1),          # MQA, window 1 (diagonal only)
+    ([200, 385], 4, 2, True, True, 200),
+    ([200], 4, 1, True, False, 0),             # no mask (the page's pseudocode)
+    ([5, 0, 7, 130], 4, 2, True, True, 0),     # an empty sequence in the middle
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("lengths,h_q,h_kv,packed,causal,window", CASES)
+def test_small_parity(dtype, lengths, h_q, h_kv, packed, causal, window):
+    prob = inputs.random_problem(11, lengths, h_q, h_kv, 64, dtype=dtype, packed=packed,
+                                 sink_scale=2.0)
+    _check(prob, dtype, causal=causal, window=window)
+
+
+def test_large_logits_and_extreme_sinks():
+    """Q, K scaled x4 (logit std ~16) with sinks in [-10, 10], and sinks of
+    +-30 that make rows sink-dominated or sink-negligible."""
+    prob = inputs.random_problem(5, [777], 8, 2, 64, dtype=torch.bfloat16, qk_gain=4.0)
+    prob["sinks"] = torch.linspace(-10, 10, 8)
+    _check(prob, torch.bfloat16, scale=0.125)
+    prob["sinks"] = torch.tensor([30.0, -30.0] * 4)
+    o, lse, *_ = _check(prob, torch.bfloat16, scale=0.125)
+    # sink-dominated heads: O ~ 0, LSE ~ S_h
+    assert float(o[:, 0::2].abs().max()) < 2e-2
+    assert float((lse[0::2] - 30.0).abs().max()) < 1e-3
+
+
+def test_minus_infinity_sink_is_standard_attention():
+    """S_h = -inf takes no probability mass (section "标准注意力机制回顾" form)."""
+    for dtype in (torch.bfloat16, torch.float32):
+        prob = inputs.random_problem(12, [300, 77], 8, 2, 64, dtype=dtype)
+        prob["sinks"] = torch.full((8,), float("-inf"))
+        got = _check(prob, dtype, window=100)
+        assert torch.all(got[5] == 0)
+
+
+def test_window_wider_than_sequence_equals_causal():
+    prob = inputs.random_problem(3, [300, 41], 8, 2, 64)
+    a = _run(prob, window=0)
+    b = _run(prob, window=4096)
+    for x, y in zip(a, b):
+        torch.testing.assert_close(x, y, rtol=0, atol=0)
+
+
+def test_packed_single_sequence_equals_padded():
+    prob = inputs.random_problem(4, [384, 384], 8, 2, 64, packed=False)
+    a = _run(prob)
+    packed = {k: (v.reshape(-1, *v.shape[2:]) if k in ("q", "k", "v", "dout") else v)
+              for k, v in prob.items()}
+    packed["cu_seqlens"] = torch.tensor([0, 384, 768], dtype=torch.int32)
+    b = _run(packed)
+    for x, y in zip(a[:1] + a[2:5], b[:1] + b[2:5]):
+        torch.testing.assert_close(x.reshape(y.shape), y, rtol=0, atol=0)
+    torch.testing.assert_close(a[1], b[1], rtol=0, atol=0)
+    torch.testing.assert_close(a[5], b[5], rtol=0, atol=0)
+
+
+def test_sink_gradient_is_deterministic():
+    prob = inputs.random_problem(6, [1000, 531], 8, 2, 64)
+    first = _run(prob)[5]
+    for _ in range(3):
+        torch.testing.assert_close(_run(prob)[5], first, rtol=0, atol=0)
+
+
+def test_empty_input():
+    q = torch.empty(0, 4, 64, dtype=torch.bfloat16, device=DEV)
+    k = torch.empty(0, 1, 64, dtype=torch.bfloat16, device=DEV)
+    sinks = torch.randn(4, device=DEV)
+    cu = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, lse = sa.sink_attn_fwd(q, k, k, sinks, cu, max_seqlen=0)
+    dq, dk, dv, ds = sa.sink_attn_bwd(q, k, k, sinks, o, lse, q, cu, max_seqlen=0)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and lse.numel() == 0
+    assert torch.all(ds == 0)
+
+
+def test_sequence_longer_than_max_seqlen_is_flagged():
+    """Rows past max_seqlen are not computed and the device flag reports it."""
+    prob = inputs.random_problem(8, [100, 300], 4, 1, 64)
+    d = {k: v.to(DEV) for k, v in prob.items()}
+    p = sa.make_params(d["q"], d["k"], d["cu_seqlens"], max_seqlen=256)
+    ws = torch.empty(sa.sink_attn_workspace_bytes(p, False), dtype=torch.uint8, device=DEV)
+    sa.sink_attn_fwd(d["q"], d["k"], d["v"], d["sinks"], d["cu_seqlens"], params=p, workspace=ws)
+    st, flags = sa.sink_attn_fetch_device_error(ws)
+    assert st == _abi.SINK_ERR_DEVICE and flags == 2
+    st, flags = sa.sink_attn_fetch_device_error(ws)  # cleared by the read
+    assert st == _abi.SINK_OK and flags == 0
+
+
+def test_host_pointer_rejected_before_launch():
+    prob = inputs.random_problem(9, [64], 4, 1, 64)
+    d = {k: (v.to(DEV) if v is not None else None) for k, v in prob.items()}
+    p = sa.make_params(d["q"], d["k"], d["cu_seqlens"], max_seqlen=64)
+    ws = torch.empty(sa.sink_attn_workspace_bytes(p, False), dtype=torch.uint8, device=DEV)
+    host_q = prob["q"].contiguous()
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(4, 64, device=DEV)
+    st = _abi.lib().sink_attn_fwd(
+        __import__("ctypes").byref(p), sa._ptr(host_q), sa._ptr(d["k"]), sa._ptr(d["v"]),
+        sa._ptr(d["sinks"]), sa._ptr(d["cu_seqlens"]), sa._ptr(o), sa._ptr(lse), sa._ptr(ws),
+        ws.numel(), sa._stream(None, d["q"].device))
+    assert st == _abi.SINK_ERR_INVALID_ARG
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    prob = inputs.random_problem(10, [333], 8, 2, 64)
+    d = {k: (v.to(DEV) if v is not None else None) for k, v in prob.items()}
+    q = d["q"].clone().requires_grad_()
+    k = d["k"].clone().requires_grad_()
+    v = d["v"].clone().requires_grad_()
+    s = d["sinks"].clone().requires_grad_()
+    o = sa.sink_attention(q, k, v, s, d["cu_seqlens"], max_seqlen=333)
+    o.backward(d["dout"])
+    ref = _run(prob)
+    torch.testing.assert_close(o.detach(), ref[0], rtol=0, atol=0)
+    for g, r in zip((q.grad, k.grad, v.grad, s.grad), ref[2:]):
+        torch.testing.assert_close(g, r, rtol=0, atol=0)
