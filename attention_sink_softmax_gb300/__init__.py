@@ -27,7 +27,8 @@ from ._abi import SinkAttnError, SinkAttnParams, lib, status_str  # noqa: F401
 __all__ = [
     "SinkAttnParams", "SinkAttnError", "make_params", "sink_attn_workspace_bytes",
     "sink_attn_fwd", "sink_attn_bwd", "sink_attn_bwd_preprocess", "sink_attn_bwd_main",
-    "sink_attn_fetch_device_error", "sink_attn_status_str", "sink_attn_kernel_launches",
+    "sink_attn_fetch_device_error", "sink_attn_bwd_preprocess_noalloc",
+    "sink_attn_noalloc_scratch_bytes", "sink_attn_status_str", "sink_attn_kernel_launches",
     "sink_attn_version",
     "sink_attention", "SinkAttentionFunction",
 ]
@@ -199,6 +200,33 @@ def sink_attn_bwd_main(params, q, k, v, lse, delta, dout, cu_seqlens=None, *, dq
                                   _stream(stream, q.device))
     _abi.check(st, "sink_attn_bwd_main")
     return dq, dk, dv
+
+
+def sink_attn_bwd_preprocess_noalloc(params, sinks, o, lse, dout, *, delta=None, dsinks=None,
+                                     stream=None):
+    """Backward step 1 with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot obtain scratch device memory; see
+    sink_attn_bwd_preprocess_noalloc in include/sink_attn.h for the size limit
+    and the rule that overlapping calls race. Returns (delta, dsinks); pass
+    preallocated ``delta``/``dsinks`` to allocate nothing here either.
+    """
+    _need_cuda("o", o)
+    _need_cuda("dout", dout, o.dtype)
+    _need_cuda("lse", lse, torch.float32)
+    _need_cuda("sinks", sinks, torch.float32)
+    if delta is None:
+        delta = torch.empty((params.h_q, params.total_tokens), dtype=torch.float32, device=o.device)
+    dsinks = torch.empty_like(sinks) if dsinks is None else dsinks
+    st = lib().sink_attn_bwd_preprocess_noalloc(ctypes.byref(params), _ptr(sinks), _ptr(o),
+                                                _ptr(lse), _ptr(dout), _ptr(delta), _ptr(dsinks),
+                                                _stream(stream, o.device))
+    _abi.check(st, "sink_attn_bwd_preprocess_noalloc")
+    return delta, dsinks
+
+
+def sink_attn_noalloc_scratch_bytes() -> int:
+    return int(lib().sink_attn_noalloc_scratch_bytes())
 
 
 def sink_attn_fetch_device_error(workspace: torch.Tensor, stream=None):

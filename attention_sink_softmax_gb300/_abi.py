@@ -19,6 +19,7 @@ SINK_ERR_CUDA = 3
 SINK_ERR_WORKSPACE = 4
 SINK_ERR_TIMEOUT = 5
 SINK_ERR_DEVICE = 6
+SINK_ERR_SCRATCH_LIMIT = 7
 
 SINK_BF16 = 0
 SINK_FP32 = 1
@@ -31,6 +32,8 @@ EXPORTS = (
     "sink_attn_bwd_preprocess",
     "sink_attn_bwd_main",
     "sink_attn_fetch_device_error",
+    "sink_attn_bwd_preprocess_noalloc",
+    "sink_attn_noalloc_scratch_bytes",
     "sink_attn_status_str",
     "sink_attn_kernel_launches",
     "sink_attn_version",
@@ -97,6 +100,10 @@ def lib():
             L.sink_attn_fetch_device_error.argtypes = [_P, ctypes.c_size_t, _P,
                                                        ctypes.POINTER(ctypes.c_uint32)]
             L.sink_attn_fetch_device_error.restype = ctypes.c_int
+            L.sink_attn_bwd_preprocess_noalloc.argtypes = [_PP] + [_P] * 6 + [_P]
+            L.sink_attn_bwd_preprocess_noalloc.restype = ctypes.c_int
+            L.sink_attn_noalloc_scratch_bytes.argtypes = []
+            L.sink_attn_noalloc_scratch_bytes.restype = ctypes.c_size_t
             L.sink_attn_status_str.argtypes = [ctypes.c_int]
             L.sink_attn_status_str.restype = ctypes.c_char_p
             L.sink_attn_kernel_launches.argtypes = []

@@ -239,6 +239,7 @@ const char* sink_attn_status_str(sink_status_t status) {
         case SINK_ERR_WORKSPACE: return "workspace missing or too small";
         case SINK_ERR_TIMEOUT: return "a bounded device wait gave up";
         case SINK_ERR_DEVICE: return "device flagged an input condition";
+        case SINK_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of the no-allocation entry point";
     }
     return "unknown status";
 }

@@ -75,7 +75,8 @@ typedef enum {
     SINK_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     SINK_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than sink_attn_workspace_bytes */
     SINK_ERR_TIMEOUT = 5,      /* a kernel's bounded wait gave up (reported by fetch_device_error) */
-    SINK_ERR_DEVICE = 6        /* another condition flagged on the device (see fetch_device_error) */
+    SINK_ERR_DEVICE = 6,       /* another condition flagged on the device (see fetch_device_error) */
+    SINK_ERR_SCRATCH_LIMIT = 7 /* problem too large for the fixed scratch of a _noalloc entry point */
 } sink_status_t;
 
 typedef enum { SINK_BF16 = 0, SINK_FP32 = 1 } sink_dtype_t;
@@ -146,6 +147,30 @@ SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
  * raw flag bits. */
 SINK_API sink_status_t sink_attn_fetch_device_error(void* workspace, size_t workspace_bytes,
                                            sink_stream_t stream, uint32_t* flags_out);
+
+/* Backward step 1 without a workspace argument. No counterpart on the page:
+ * this entry point exists for callers that are given their input and output
+ * buffers but cannot obtain any other device memory (a plugin inside a host
+ * framework that owns all device memory and offers no scratch allocator, or a
+ * path where a cudaMalloc would synchronise the device or fail because a
+ * caching allocator already holds the memory). It computes exactly what
+ * sink_attn_bwd_preprocess computes, keeping its per-chunk dS_h partial sums
+ * in a fixed device array inside the library (sink_attn_noalloc_scratch_bytes,
+ * 1 MiB, held by every GPU that loads the library until the process exits).
+ * It allocates and frees nothing. Limits: h_q * ceil(T / 256) partials must
+ * fit the array, else SINK_ERR_SCRATCH_LIMIT is returned before anything is
+ * enqueued. All calls on a device share the array, so calls whose work
+ * overlaps on the GPU race; order them on one stream. The first call on each
+ * device (with that device current) looks up the array's device address;
+ * make that first call before any stream capture. */
+SINK_API sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t* params,
+                                                        const float* sinks, const void* o,
+                                                        const float* lse, const void* dout,
+                                                        float* delta, float* dsinks,
+                                                        sink_stream_t stream);
+
+/* Size in bytes of the fixed scratch array used by the _noalloc entry point. */
+SINK_API size_t sink_attn_noalloc_scratch_bytes(void);
 
 /* Static description of a status code. Never NULL. */
 SINK_API const char* sink_attn_status_str(sink_status_t status);
