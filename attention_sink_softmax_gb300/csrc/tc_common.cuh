@@ -1,0 +1,57 @@
+// tc_common.cuh - pieces shared by the tensor-core kernels: bounded mbarrier
+// waits driven by the global nanosecond timer, and the TMA tensor-map builder
+// for [T, H, 64] bf16 tensors.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace sinkattn {
+namespace tc {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase; on timeout raises the timeout flag and
+// the CTA abort word. Returns false if the wait did not complete (timeout, or
+// another role of the CTA already gave up).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint32_t* flags,
+                                           volatile int* abort_word) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_word) return false;
+        if (now_ns() - t0 > kWaitLimitNs) {
+            atomicOr(flags, kFlagTimeout);
+            *abort_word = 1;
+            return false;
+        }
+    }
+}
+
+// Time-bounded wait that ignores the abort word: used only to let copies or
+// MMAs that were already issued finish before shared or tensor memory is
+// given up.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = now_ns();
+    while (!mbar_try_wait(bar, parity) && now_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
+}  // namespace tc
+
+// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token) with 128-byte
+// swizzle; box = box_rows tokens x 1 head x 64. Returns false if the driver's
+// encoder is unavailable or rejects the tensor.
+bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows);
+
+}  // namespace sinkattn

@@ -1,0 +1,421 @@
+// tc_fwd.cu - sink-attention forward on the sm_103a tensor cores.
+//
+// What it computes (page "惊爆！GPT-OSS-20B强化学习，训练速度狂飙、超稳定！",
+// sections "GPT-OSS中的带注意力槽的注意力机制" and "数学公式深入解读"): per row,
+// softmax over the allowed scores plus the head's sink logit S_h, the sink
+// column dropped before the product with V; plus the row's logsumexp with the
+// sink included.
+//
+// Structure of one CTA: NT query tiles of 128 rows that share a key/value
+// head (NT = 2 query heads of one GQA group when the group size is even), so
+// every K/V tile fetched serves NT tiles.
+//   warp 4*NT      TMA producer: Q tiles once, then K and V tiles of 128 keys
+//                  through a kStages-deep ring of shared-memory buffers.
+//   warp 4*NT + 1  MMA issuer (one thread): S_t = Q_t K^T (SS, M=128 N=128
+//                  K=64) into tensor memory, then O_t += P_t V (A = P_t read
+//                  from tensor memory, M=128 N=64 K=128). Tiles alternate, so
+//                  one tile's softmax overlaps the other tile's MMAs.
+//   warps 4t..4t+3 softmax of tile t: thread r owns row r (tensor-memory lane
+//                  r). The running max starts at the sink logit and the running
+//                  sum at the sink's own term, so the sink joins the
+//                  denominator and contributes no value row. The max is only
+//                  moved (and O rescaled in tensor memory) when it grows by
+//                  more than kRescaleLog2 in log2 units; P values then stay
+//                  below 2^kRescaleLog2 and the final O / l is unchanged.
+// Tensor memory (512 columns): S_t at t*128, O_t at 256 + t*64, P_t (bf16
+// pairs) at 384 + t*64. Every mbarrier wait is bounded; a wait that gives up
+// sets the timeout flag and the CTA winds down without further work.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace sinkattn {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per block
+constexpr int kD = 64;             // head dim
+constexpr int kStages = 3;         // K/V ring depth
+constexpr uint32_t kTileBytes = kBM * kD * 2;
+constexpr float kRescaleLog2 = 8.0f;
+// Register split for two tiles (384 threads launched at kLaunchRegs each):
+// 2 softmax warpgroups x 128 x kSoftmaxRegs + 1 warpgroup x 128 x kOtherRegs
+// = 53248 + 11264 = 64512 = 384 x 168.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 88;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 384 * kLaunchRegs, "register split");
+
+template <int NT>
+constexpr int fwd_threads() { return NT * 128 + 128; }
+
+template <int NT>
+struct FwdSmem {
+    alignas(1024) __nv_bfloat16 q[NT][kBM * kD];
+    alignas(1024) __nv_bfloat16 k[kStages][kBN * kD];
+    alignas(1024) __nv_bfloat16 v[kStages][kBN * kD];
+    uint64_t q_full;
+    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t s_full[NT], p_full[NT], o_done[NT];
+    uint64_t drained;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(fwd_threads<NT>(), 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const Problem P,
+              const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
+              float* __restrict__ lse, uint32_t* flags) {
+    extern __shared__ uint8_t smem_raw[];
+    FwdSmem<NT>& sm = *reinterpret_cast<FwdSmem<NT>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rb = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+    const int seq = blockIdx.z;
+    const int h0 = blockIdx.y * NT;
+    int start, L;
+    seq_bounds(P, seq, start, L);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && L > P.max_seqlen) atomicOr(flags, kFlagSeqTooLong);
+    const int r0 = rb * kBM;
+    if (r0 >= L) return;  // uniform for the whole CTA, before any barrier or TMEM use
+
+    int kb_lo = 0, kb_hi = (L - 1) / kBN;
+    if (P.causal) {
+        kb_hi = rb;
+        if (P.window > 0) kb_lo = max(0, r0 - P.window + 1) / kBN;
+    }
+    const int nblk = kb_hi - kb_lo + 1;
+    const int hk = h0 / P.group;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.p_full[t], 128);
+            mbar_init(&sm.o_done[t], 1);
+        }
+        mbar_init(&sm.drained, 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc<512>(&sm.tmem_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_slot;
+    volatile int* abort_word = &sm.abort_flag;
+
+    if (warp < 4 * NT) {
+        if (NT == 2) regs_increase<kSoftmaxRegs>();
+        // ------------------------------------------------------------ softmax warpgroup t
+        const int t = warp / 4;
+        const int wq = warp % 4;
+        const int r = wq * 32 + lane;
+        const int h = h0 + t;
+        const int row = r0 + r;
+        const bool valid = row < L;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 64;
+        const uint32_t tP = tmem + lane_off + 384 + t * 64;
+        const float sc = P.scale_log2;
+        float m = __ldg(sinks + h) * kLog2e;  // running max in log2 units, seeded by the sink
+        float l = m == -INFINITY ? 0.f : 1.f;  // running sum, seeded by the sink's own term
+        bool ok = true;
+        for (int i = 0; i < nblk; ++i) {
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], i & 1, flags, abort_word));
+            // S_t(i) was committed after PV(t, i-1), so that product has finished
+            // too: O_t and P_t are free to touch
+            if (ok && i > 0)
+                ok = __all_sync(0xffffffffu,
+                                wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+            {
+                uint32_t a[32], b[32], c[32], d[32];
+                tmem_ld32(tS + 0, a);
+                tmem_ld32(tS + 32, b);
+                tmem_ld32(tS + 64, c);
+                tmem_ld32(tS + 96, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = __uint_as_float(a[j]);
+                    s[32 + j] = __uint_as_float(b[j]);
+                    s[64 + j] = __uint_as_float(c[j]);
+                    s[96 + j] = __uint_as_float(d[j]);
+                }
+            }
+            const int kp0 = (kb_lo + i) * kBN;  // first key position of the block
+            const bool need_mask =
+                P.causal ? (kp0 + kBN - 1 > r0 ||
+                            (P.window > 0 && kp0 < r0 + kBM - P.window))
+                         : (kp0 + kBN > L);
+            if (need_mask) {
+                const int lo = P.causal && P.window > 0 ? row - P.window + 1 : INT_MIN;
+                const int hi = P.causal ? min(row, L - 1) : L - 1;
+#pragma unroll
+                for (int j = 0; j < 128; ++j) {
+                    const int kp = kp0 + j;
+                    if (kp < lo || kp > hi) s[j] = -INFINITY;
+                }
+            }
+            float mx8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx8[u] = s[u];
+#pragma unroll
+            for (int j = 8; j < 128; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float mx = smax * sc;
+            const bool upd = i == 0 ? mx > m : mx > m + kRescaleLog2;
+            const float m_new = upd ? mx : m;
+            const float corr = upd ? (m == -INFINITY ? 0.f : fast_exp2(m - m_new)) : 1.f;
+            const float mref = m_new == -INFINITY ? 0.f : m_new;
+            float rs8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) {
+                    const float p0 = fast_exp2(fmaf(s[64 * half + j], sc, -mref));
+                    const float p1 = fast_exp2(fmaf(s[64 * half + j + 1], sc, -mref));
+                    rs8[(j >> 1) & 7] += p0 + p1;
+                    pk[j >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tP + 32 * half, pk);
+            }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
+                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            if (i > 0 && __any_sync(0xffffffffu, upd)) {
+                uint32_t oa[32], ob[32];
+                tmem_ld32(tO, oa);
+                tmem_ld32(tO + 32, ob);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    oa[j] = __float_as_uint(__uint_as_float(oa[j]) * corr);
+                    ob[j] = __float_as_uint(__uint_as_float(ob[j]) * corr);
+                }
+                tmem_st32(tO, oa);
+                tmem_st32(tO + 32, ob);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[t]);
+            l = l * corr + rs;
+            m = m_new;
+        }
+        if (ok)
+            ok = __all_sync(0xffffffffu,
+                            wait_phase(&sm.o_done[t], (nblk - 1) & 1, flags, abort_word));
+        if (ok) {
+            tc_fence_after();
+            uint32_t oa[32], ob[32];
+            tmem_ld32(tO, oa);
+            tmem_ld32(tO + 32, ob);
+            tmem_ld_wait();
+            if (valid) {
+                const float inv = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * kD);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(oa[8 * j + 0]) * inv, __uint_as_float(oa[8 * j + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(oa[8 * j + 2]) * inv, __uint_as_float(oa[8 * j + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(oa[8 * j + 4]) * inv, __uint_as_float(oa[8 * j + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(oa[8 * j + 6]) * inv, __uint_as_float(oa[8 * j + 7]) * inv);
+                    dst[j] = w;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ob[8 * j + 0]) * inv, __uint_as_float(ob[8 * j + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(ob[8 * j + 2]) * inv, __uint_as_float(ob[8 * j + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(ob[8 * j + 4]) * inv, __uint_as_float(ob[8 * j + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(ob[8 * j + 6]) * inv, __uint_as_float(ob[8 * j + 7]) * inv);
+                    dst[4 + j] = w;
+                }
+                lse[(size_t)h * P.total + start + row] = (m + __log2f(l)) * kLn2;
+            }
+        }
+        } else {
+        if (NT == 2) regs_decrease<kOtherRegs>();
+        if (warp == 4 * NT) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                mbar_arrive_expect_tx(&sm.q_full, NT * kTileBytes);
+                for (int t = 0; t < NT; ++t) tma_load_3d(sm.q[t], &tmQ, &sm.q_full, 0, h0 + t, start + r0);
+                int issued = 0;
+                for (int i = 0; i < nblk; ++i) {
+                    const int st = i % kStages;
+                    if (i >= kStages &&
+                        !wait_phase(&sm.kv_empty[st], ((i / kStages) - 1) & 1, flags, abort_word))
+                        break;
+                    const int kpos = start + (kb_lo + i) * kBN;
+                    mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                    tma_load_3d(sm.k[st], &tmK, &sm.k_full[st], 0, hk, kpos);
+                    mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                    tma_load_3d(sm.v[st], &tmV, &sm.v_full[st], 0, hk, kpos);
+                    issued = i + 1;
+                }
+                // copies still in flight must land before the CTA's shared memory goes away
+                drain_phase(&sm.q_full, 0);
+                for (int i = max(0, issued - kStages); i < issued; ++i) {
+                    const int st = i % kStages;
+                    drain_phase(&sm.k_full[st], (i / kStages) & 1);
+                    drain_phase(&sm.v_full[st], (i / kStages) & 1);
+                }
+            }
+        } else if (warp == 4 * NT + 1) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q, K both K-major
+                constexpr uint32_t idO = idesc_bf16(kBM, kD, 0, 1);   // P from TMEM, V MN-major
+                uint64_t dq[NT];
+                for (int t = 0; t < NT; ++t) dq[t] = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
+                bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
+                          wait_phase(&sm.k_full[0], 0, flags, abort_word);
+                if (ok) {
+                    tc_fence_after();
+                    const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+                    for (int t = 0; t < NT; ++t) {
+                        for (int kk = 0; kk < kD / 16; ++kk)
+                            mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                        mma_commit(&sm.s_full[t]);
+                    }
+                }
+                for (int i = 0; ok && i < nblk; ++i) {
+                    const int st = i % kStages;
+                    if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
+                    const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
+                    for (int t = 0; t < NT; ++t) {
+                        if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
+                        tc_fence_after();
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8,
+                                   dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
+                        mma_commit(&sm.o_done[t]);
+                        if (i + 1 < nblk) {
+                            const int st1 = (i + 1) % kStages;
+                            if (t == 0) {
+                                if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags,
+                                                      abort_word)))
+                                    break;
+                                tc_fence_after();
+                            }
+                            const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st1]), 16, 1024);
+                            for (int kk = 0; kk < kD / 16; ++kk)
+                                mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                            mma_commit(&sm.s_full[t]);
+                        }
+                    }
+                    mma_commit(&sm.kv_empty[st]);
+                }
+                // every MMA issued above must finish before tensor memory is released
+                mma_commit(&sm.drained);
+                drain_phase(&sm.drained, 0);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<512>(tmem);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 128 tokens x 1 head.
+bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_fwd_supported(const Problem& P, bool bf16) {
+    return bf16 && P.head_dim == kD && encode_fn() != nullptr && P.total > 0;
+}
+
+size_t tc_fwd_workspace_bytes(const Problem&, bool) { return 0; }
+
+template <int NT>
+static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const float* sinks, void* o, float* lse,
+                              uint32_t* flags, cudaStream_t st) {
+    if (NT == 2) {
+        // the register split above is only safe at exactly this launch value
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<NT>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
+    const size_t smem = sizeof(FwdSmem<NT>) + 1024;
+    cudaError_t attr_err = cudaFuncSetAttribute(
+        fwd_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid((P.max_seqlen + kBM - 1) / kBM, P.h_q / NT, P.nseq);
+    fwd_tc_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
+                                                         (__nv_bfloat16*)o, lse, flags);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
+                   const float* sinks, void* o, float* lse, uint32_t* flags, void*,
+                   cudaStream_t st) {
+    if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
+    CUtensorMap mq, mk, mv;
+    if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM) ||
+        !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
+        !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN))
+        return cudaErrorInvalidValue;
+    if (P.group % 2 == 0) return launch_fwd<2>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    return launch_fwd<1>(P, mq, mk, mv, sinks, o, lse, flags, st);
+}
+
+}  // namespace sinkattn

@@ -168,6 +168,19 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- register split
+// Executed by every warp of a warpgroup. The block's register pool is its
+// launch value (threads x registers per thread at launch); increases must be
+// covered by matching decreases elsewhere in the block.
+template <int kRegs>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format):
 //   [0,14)  start address >> 4      [16,30) leading-dimension byte offset >> 4
