@@ -106,37 +106,88 @@ simt_fwd_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
 // ---------------------------------------------------------------------------
 // Backward step 1: delta = rowsum(dO * O) in [h_q, T] and per-chunk partials of
 // sum_t exp(S_h - LSE_t) * delta_t. One block = one head x kPreTokens tokens;
-// 8 lanes share one 64-wide row (16-byte loads for bf16).
+// 8 lanes share one 64-wide row, each lane one 16-byte (bf16) or 32-byte
+// (fp32) piece. All of a thread's loads are issued before any is used, so
+// every thread keeps kPreIters rows of O and dO in flight (memory-bound step).
 constexpr int kPreTokens = 256;
 constexpr int kPreThreads = 256;
+
+// 8 consecutive elements of T as 16-byte words
+template <typename T>
+struct Piece8 {
+    static constexpr int kWords = (int)sizeof(T) * 8 / 16;
+    uint4 w[kWords];
+};
+
+template <typename T>
+__device__ __forceinline__ Piece8<T> load_piece(const T* p) {
+    Piece8<T> r;
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < Piece8<T>::kWords; ++i) r.w[i] = __ldg(q + i);
+    return r;
+}
+
+__device__ __forceinline__ float dot_piece(const Piece8<__nv_bfloat16>& a,
+                                           const Piece8<__nv_bfloat16>& b) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a.w[0]);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b.w[0]);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 u = __bfloat1622float2(x[i]), v = __bfloat1622float2(y[i]);
+        s = fmaf(u.x, v.x, s);
+        s = fmaf(u.y, v.y, s);
+    }
+    return s;
+}
+
+__device__ __forceinline__ float dot_piece(const Piece8<float>& a, const Piece8<float>& b) {
+    const float* x = reinterpret_cast<const float*>(&a.w[0]);
+    const float* y = reinterpret_cast<const float*>(&b.w[0]);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = fmaf(x[i], y[i], s);
+    return s;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kPreThreads)
 preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restrict__ dout,
                   const float* __restrict__ lse, const float* __restrict__ sinks,
                   float* __restrict__ delta, float* __restrict__ partial) {
-    constexpr int kLanes = 8;                 // threads per row
-    constexpr int kPer = kD / kLanes;         // elements per thread
+    constexpr int kLanes = 8;  // threads per row
+    constexpr int kPer = kD / kLanes;
     constexpr int kRowsPerIter = kPreThreads / kLanes;
+    constexpr int kIters = kPreTokens / kRowsPerIter;
     __shared__ float warp_sum[kPreThreads / 32];
     const int h = blockIdx.y;
     const int t0 = blockIdx.x * kPreTokens;
     const int sub = threadIdx.x % kLanes;
+    const int r0 = threadIdx.x / kLanes;
     const float sink = __ldg(sinks + h);
-    float mine = 0.f;  // this row-group's running sum, added in token order
-    for (int r = threadIdx.x / kLanes; r < kPreTokens; r += kRowsPerIter) {
-        const int t = t0 + r;
-        float dsum = 0.f;
+    Piece8<T> po[kIters], pd[kIters];
+    float lz[kIters];
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int t = t0 + r0 + it * kRowsPerIter;
         if (t < total) {
             const size_t off = ((size_t)t * h_q + h) * kD + sub * kPer;
-#pragma unroll
-            for (int c = 0; c < kPer; ++c) dsum = fmaf(to_f32(o[off + c]), to_f32(dout[off + c]), dsum);
+            po[it] = load_piece(o + off);
+            pd[it] = load_piece(dout + off);
+            lz[it] = __ldg(lse + (size_t)h * total + t);
         }
+    }
+    float mine = 0.f;  // this row-group's running sum, added in token order
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int t = t0 + r0 + it * kRowsPerIter;
+        float dsum = t < total ? dot_piece(po[it], pd[it]) : 0.f;
 #pragma unroll
         for (int w = kLanes / 2; w >= 1; w >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, w);
         if (t < total) {
             if (sub == 0) delta[(size_t)h * total + t] = dsum;
-            mine += expf(sink - lse[(size_t)h * total + t]) * dsum;
+            mine += expf(sink - lz[it]) * dsum;
         }
     }
     // fixed-order reduction: lanes 0, 8, 16, 24 of each warp, then warps in order

@@ -231,6 +231,46 @@ def run_reference(args, w, window):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, lse, dq, dk, dv,
+            dsinks, work, flops_step):
+    """Same step through the public API with pinned host buffers: inputs copied
+    in and every output copied back inside the timed region."""
+    import attention_sink_softmax_gb300 as sa
+    host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv),
+                             ("dsinks", dsinks))}
+    dev_in = {"q": q, "k": k, "v": v, "sinks": sinks, "dout": dout}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
+        sa.sink_attn_bwd(q, k, v, sinks, o, lse, dout, cu, dq=dq, dk=dk, dv=dv, dsinks=dsinks,
+                         workspace=work, params=p)
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dsinks", dsinks)):
+            host_out[n].copy_(t, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    e2e_value = flops_step * ws / (ms_e2e / 1000) / 1e12
+    return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+
+
 def run_gpu(args, w, window):
     import attention_sink_softmax_gb300 as sa
 
@@ -302,36 +342,10 @@ def run_gpu(args, w, window):
     value = flops_step * ws / (ms / 1000) / 1e12
 
     # ---- end to end through the public API with host buffers (pinned)
-    host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
-    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv),
-                             ("dsinks", dsinks))}
-    dev_in = {"q": q, "k": k, "v": v, "sinks": sinks, "dout": dout}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-
-    def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
-        sa.sink_attn_bwd(q, k, v, sinks, o, lse, dout, cu, dq=dq, dk=dk, dv=dv, dsinks=dsinks,
-                         workspace=work, params=p)
-        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dsinks", dsinks)):
-            host_out[n].copy_(t, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier(ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(ws)
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    e2e_value = flops_step * ws / (ms_e2e / 1000) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, lse, dq,
+                      dk, dv, dsinks, work, flops_step)
 
     pk, pk_src = peaks()
     # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop
@@ -361,8 +375,7 @@ def run_gpu(args, w, window):
                         "source": pk_src},
         "stages_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1], "bwd_main": stage_ms[2]},
         "clocks": clk.summary(),
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "e2e": e2e,
         "gpu_launches": int(launches),
         "roofline": roofline,
     }
@@ -386,6 +399,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, help="workload index 0..4")
     ap.add_argument("--window", type=int, default=None, help="override the workload's window")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     args = ap.parse_args()
     w = inputs.workload(args.config)
     window = w.window if args.window is None else args.window
