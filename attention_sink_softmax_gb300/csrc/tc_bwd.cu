@@ -12,21 +12,29 @@
 //
 // One CTA = one key block of 128 keys of one key/value head of one sequence;
 // it walks every (query head of the group, query block of 128 rows) that can
-// see the block, accumulating dK and dV in tensor memory, and adds each dQ
-// block into an fp32 accumulator in the workspace.
-//   warps 0-7    two elementwise warpgroups: thread = key (tensor-memory lane),
-//                warpgroup w takes query rows [64w, 64w+64) of the block.
-//                P^T goes to tensor memory (A operand of dV), dS^T to shared
-//                memory in a layout that is the K-major A operand of dK and,
-//                read the other way, the MN-major A operand of dQ.
-//   warp 8       TMA producer: K, V once; Q, dO (+ LSE, delta) per step through
-//                a 2-deep ring.
-//   warp 9       MMA issuer (one thread): S^T = K Q^T and dP^T = V dO^T for the
-//                next step as soon as the elementwise warps have read the
-//                current ones, then dV += P^T dO, dK += dS^T Q, dQ = dS K.
-//   warps 12-15  dQ drain: tensor memory -> fp32 vector atomics.
-// Tensor memory: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383,
-// dQ 384..447, P^T (bf16 pairs) 448..511.
+// see the block ("steps"), accumulating dK and dV in tensor memory, and adds
+// each step's dQ block into an fp32 accumulator in the workspace.
+//
+// Operand placement. On this tensor core an MMA whose A operand comes from
+// tensor memory issues about twice as fast as one reading A from shared
+// memory, so every product whose A operand can live in tensor memory does:
+//   S^T  = K Q^T     A = K    (tensor memory, loaded once)    B = Q  (smem)
+//   dP^T = V dO^T    A = V    (tensor memory, loaded once)    B = dO (smem)
+//   dV  += P^T dO    A = P^T  (tensor memory, from registers) B = dO
+//   dK  += dS^T Q    A = dS^T (tensor memory, from registers) B = Q
+//   dQ   = dS K      A = dS   (smem: needs query rows as M)   B = K  (smem)
+// S^T and dP^T share one 128-column region: the elementwise warps read S^T
+// into registers, then dP^T is computed into the same columns while they
+// exponentiate. Per step the tensor pipe runs dP(i), the gradients of step
+// i-1, then S(i+1), so the elementwise work of step i overlaps the gradient
+// products of step i-1.
+//
+// Warps: 0-7 elementwise (thread = key = tensor-memory lane; warpgroup w takes
+// query rows [64w, 64w+64) of the step); 8 producer (TMA for K, Q, dO and
+// cp.async for the step's LSE and delta rows, through a kQStages ring); 9 MMA
+// issuer (one thread); 12-15 dQ drain (tensor memory -> shared staging -> TMA
+// bulk reduce-add). Tensor memory: S^T/dP^T 0..127, dV 128..191, dK
+// 192..255, dQ 256..319, K 320..351, V 352..383, P^T 384..447, dS^T 448..511.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -45,33 +53,35 @@ using namespace tc;
 constexpr int kBN = 128;  // keys per CTA
 constexpr int kBM = 128;  // query rows per step
 constexpr int kD = 64;
-constexpr int kQStages = 2;
+constexpr int kQStages = 3;
 constexpr uint32_t kTileBytes = kBM * kD * 2;
 constexpr int kThreads = 512;
 // Register split (launch: 512 threads x 128): 2 elementwise warpgroups x 128
-// x 176 + producer/MMA warpgroup x 128 x 56 + dQ warpgroup x 128 x 96
-// = 45056 + 7168 + 12288 = 64512 <= 65536.
+// x 192 + producer/MMA warpgroup x 128 x 64 + dQ warpgroup x 128 x 64
+// = 49152 + 8192 + 8192 = 65536.
 constexpr int kLaunchRegs = 128;
-constexpr int kEltRegs = 176;
-constexpr int kCtlRegs = 56;
-constexpr int kDqRegs = 96;
+constexpr int kEltRegs = 192;
+constexpr int kCtlRegs = 64;
+constexpr int kDqRegs = 64;
 static_assert(2 * 128 * kEltRegs + 128 * kCtlRegs + 128 * kDqRegs <= kThreads * kLaunchRegs,
               "register split");
 
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColP = 448;
+constexpr uint32_t kColSdP = 0, kColDV = 128, kColDK = 192, kColDQ = 256, kColK = 320,
+                   kColV = 352, kColP = 384, kColDS = 448;
 
 struct BwdSmem {
-    alignas(1024) __nv_bfloat16 k[kBN * kD];
-    alignas(1024) __nv_bfloat16 v[kBN * kD];
+    alignas(1024) __nv_bfloat16 k[kBN * kD];  // B operand of dQ
     alignas(1024) __nv_bfloat16 q[kQStages][kBM * kD];
     alignas(1024) __nv_bfloat16 dout[kQStages][kBM * kD];
-    // dS^T: two 16 KB atoms (query rows 0..63 and 64..127), each 128 keys x 128 bytes
+    // dS: two 16 KB atoms (query rows 0..63 and 64..127), each 128 keys x 128 bytes
     alignas(1024) uint8_t ds[2][kBN * 128];
-    float lse2[kQStages][kBM];  // LSE * log2(e); +inf marks rows outside the sequence
-    float delta[kQStages][kBM];
-    uint64_t kv_full;
+    // dQ block staged for the bulk reduce: columns 0..31 and 32..63, 128 rows x 128 bytes
+    alignas(1024) uint8_t dq_stage[2][kBM * 128];
+    alignas(16) float lse[kQStages][kBM];  // rows past the sequence hold a clamped copy
+    alignas(16) float delta[kQStages][kBM];
+    uint64_t k_full, kv_tmem;
     uint64_t q_full[kQStages], q_empty[kQStages];
-    uint64_t sdp_full, s_consumed, ds_full, grads_done, dq_consumed, drained;
+    uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, grads_done, dq_consumed, drained;
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -79,6 +89,18 @@ struct BwdSmem {
 // byte offset of (row r, byte b) inside a tile of 128-byte rows with the 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128(int r, int b) {
     return (uint32_t)(r * 128 + (((b >> 4) ^ (r & 7)) << 4) + (b & 15));
+}
+
+// AND of `pred` over the 128 threads of named barrier `id` (all of them must call it)
+__device__ __forceinline__ bool vote_all_128(int id, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.cta.red.and.pred po, %2, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "r"(id)
+        : "memory");
+    return out != 0;
 }
 
 __device__ __forceinline__ uint4 pack8(const uint32_t* a, float f) {
@@ -90,9 +112,10 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* a, float f) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const Problem P, const float* __restrict__ lse, const float* __restrict__ delta,
-              float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
+              const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmDQ,
+              const Problem P, const __nv_bfloat16* __restrict__ kg,
+              const __nv_bfloat16* __restrict__ vg, const float* __restrict__ lse,
+              const float* __restrict__ delta, __nv_bfloat16* __restrict__ dk,
               __nv_bfloat16* __restrict__ dv, uint32_t* flags) {
     extern __shared__ uint8_t smem_raw[];
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(
@@ -117,13 +140,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int nsteps = nq * P.group;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm.kv_full, 1);
+        mbar_init(&sm.k_full, 1);
+        mbar_init(&sm.kv_tmem, 256);
         for (int i = 0; i < kQStages; ++i) {
             mbar_init(&sm.q_full[i], 1 + 32);
             mbar_init(&sm.q_empty[i], 1);
         }
-        mbar_init(&sm.sdp_full, 1);
-        mbar_init(&sm.s_consumed, 256);
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.s_loaded, 256);
+        mbar_init(&sm.dp_full, 1);
+        mbar_init(&sm.dp_loaded, 256);
         mbar_init(&sm.ds_full, 256);
         mbar_init(&sm.grads_done, 1);
         mbar_init(&sm.dq_consumed, 128);
@@ -141,55 +167,110 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (warp < 8) {
         // ------------------------------------------------------------ elementwise
         regs_increase<kEltRegs>();
-        const int w = warp / 4;         // query-row half of the block
+        const int w = warp / 4;         // query-row half of the step (and K or V at start)
         const int wq = warp % 4;
         const int kr = wq * 32 + lane;  // key within the block (tensor-memory lane)
         const int kp = k0 + kr;         // key position in the sequence
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float sc = P.scale_log2;
+        {
+            // A operands of S^T and dP^T: warpgroup 0 places this key's K row,
+            // warpgroup 1 its V row (zeros past the sequence)
+            uint32_t row[32];
+            const __nv_bfloat16* src = (w == 0 ? kg : vg) + ((size_t)(start + kp) * P.h_kv + hk) * kD;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 x = kp < L ? __ldg(reinterpret_cast<const uint4*>(src) + j) : make_uint4(0, 0, 0, 0);
+                row[4 * j] = x.x;
+                row[4 * j + 1] = x.y;
+                row[4 * j + 2] = x.z;
+                row[4 * j + 3] = x.w;
+            }
+            tmem_st32(tmem + lane_off + (w == 0 ? kColK : kColV), row);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.kv_tmem);
+        }
         bool ok = true;
         for (int it = 0; it < nsteps; ++it) {
             const int st = it % kQStages;
             const int q0 = (qb_lo + it % nq) * kBM;
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.sdp_full, it & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, it & 1, flags, abort_word));
             if (!ok) break;
             tc_fence_after();
-            const bool need_mask =
-                P.causal ? (k0 + kBN - 1 > q0 || (P.window > 0 && k0 < q0 + kBM - P.window))
-                         : (k0 + kBN > L);
-            uint32_t pp[32], pd[32];  // packed bf16 pairs of P^T and dS^T, 64 rows
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int c0 = 64 * w + 32 * ch;  // first query row of the chunk
-                uint32_t sraw[32], draw[32];
-                tmem_ld32(tmem + lane_off + kColS + c0, sraw);
-                tmem_ld32(tmem + lane_off + kColDP + c0, draw);
+            float p[64];  // P^T for this key and query rows [64w, 64w+64)
+            {
+                uint32_t s0[32], s1[32];
+                tmem_ld32(tmem + lane_off + kColSdP + 64 * w, s0);
+                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32, s1);
                 tmem_ld_wait();
+                // S^T is in registers: dP^T may now be written into the same columns
+                tc_fence_before();
+                mbar_arrive(&sm.s_loaded);
+                // P = exp2(S * scale * log2 e - LSE * log2 e), two columns per paired op
+                const uint64_t sc2 = f2_pack(sc, sc);
+                const uint64_t nlog2e2 = f2_pack(-kLog2e, -kLog2e);
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float p2[2], d2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = c0 + j + u;
-                        float p = fast_exp2(fmaf(__uint_as_float(sraw[j + u]), sc, -sm.lse2[st][c]));
-                        if (need_mask) {
-                            const int ip = q0 + c;
-                            const bool allowed =
-                                P.causal ? (kp <= ip && (P.window <= 0 || kp > ip - P.window))
-                                         : kp < L;
-                            p = allowed ? p : 0.f;
-                        }
-                        p2[u] = p;
-                        d2[u] = p * (__uint_as_float(draw[j + u]) - sm.delta[st][c]);
-                    }
-                    pp[16 * ch + j / 2] = pack_bf16x2(p2[0], p2[1]);
-                    pd[16 * ch + j / 2] = pack_bf16x2(d2[0], d2[1]);
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(&sm.lse[st][64 * w + j]);
+                    const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nlog2e2);
+                    const uint64_t nl23 = f2_mul(f2_pack(l4.z, l4.w), nlog2e2);
+                    const uint32_t* src = j < 32 ? s0 + j : s1 + (j - 32);
+                    const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), sc2, nl01);
+                    const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(src[2]), __uint_as_float(src[3])), sc2, nl23);
+                    float x0, x1, x2, x3;
+                    f2_unpack(a01, x0, x1);
+                    f2_unpack(a23, x2, x3);
+                    p[j] = fast_exp2(x0);
+                    p[j + 1] = fast_exp2(x1);
+                    p[j + 2] = fast_exp2(x2);
+                    p[j + 3] = fast_exp2(x3);
                 }
             }
-            // S^T and dP^T have been read: the next step's products may overwrite them
+            // masks (boundary steps only): causal / window / past the sequence
+            if (q0 + kBM > L ||
+                (P.causal ? (k0 + kBN - 1 > q0 || (P.window > 0 && k0 < q0 + kBM - P.window))
+                          : (k0 + kBN > L))) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const int ip = q0 + 64 * w + j;
+                    const bool allowed =
+                        ip < L && (P.causal ? (kp <= ip && (P.window <= 0 || kp > ip - P.window))
+                                            : kp < L);
+                    p[j] = allowed ? p[j] : 0.f;
+                }
+            }
+            uint32_t pp[32], pd[32];  // packed bf16 pairs of P^T and dS^T
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pp[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, it & 1, flags, abort_word));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t d[32];
+                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32 * ch, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    // dS = P (dP - delta), two columns per paired op
+                    const float4 D4 = *reinterpret_cast<const float4*>(&sm.delta[st][64 * w + 32 * ch + j]);
+                    const int c = 32 * ch + j;
+                    const uint64_t t01 = f2_sub(f2_pack(__uint_as_float(d[j]), __uint_as_float(d[j + 1])),
+                                                f2_pack(D4.x, D4.y));
+                    const uint64_t t23 = f2_sub(f2_pack(__uint_as_float(d[j + 2]), __uint_as_float(d[j + 3])),
+                                                f2_pack(D4.z, D4.w));
+                    float y0, y1, y2, y3;
+                    f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t01), y0, y1);
+                    f2_unpack(f2_mul(f2_pack(p[c + 2], p[c + 3]), t23), y2, y3);
+                    pd[16 * ch + j / 2] = pack_bf16x2(y0, y1);
+                    pd[16 * ch + j / 2 + 1] = pack_bf16x2(y2, y3);
+                }
+            }
+            // dP^T has been read: the next step's S^T may overwrite the columns
             tc_fence_before();
-            mbar_arrive(&sm.s_consumed);
-            // the previous step's gradient products read P^T and dS^T: wait for them
+            mbar_arrive(&sm.dp_loaded);
+            // the previous step's gradient products read P^T, dS^T and dS: wait for them
             if (it > 0) {
                 ok = __all_sync(0xffffffffu,
                                 wait_phase(&sm.grads_done, (it - 1) & 1, flags, abort_word));
@@ -197,7 +278,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
-            // dS^T row of this key: 64 query rows = 128 bytes of atom w
+            tmem_st32(tmem + lane_off + kColDS + 32 * w, pd);
+            // dS row of this key: 64 query rows = 128 bytes of atom w (A operand of dQ)
             uint8_t* atom = sm.ds[w];
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) {
@@ -234,33 +316,43 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ------------------------------------------------------------ dQ drain
         regs_decrease<kDqRegs>();
         const int wq = warp - 12;
-        const int r = wq * 32 + lane;  // query row within the block (tensor-memory lane)
+        const int r = wq * 32 + lane;  // query row within the step (tensor-memory lane)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const bool issuer = warp == 12 && lane == 0;
         for (int it = 0; it < nsteps; ++it) {
             const int h = hk * P.group + it / nq;
-            const int qb = qb_lo + it % nq;
-            if (!__all_sync(0xffffffffu, wait_phase(&sm.grads_done, it & 1, flags, abort_word)))
-                break;
+            const int q0 = (qb_lo + it % nq) * kBM;
+            // one decision for all four drain warps (they meet at named barriers below)
+            if (!vote_all_128(1, wait_phase(&sm.grads_done, it & 1, flags, abort_word))) break;
             tc_fence_after();
-            uint32_t a[32], b[32];
-            tmem_ld32(tmem + lane_off + kColDQ, a);
-            tmem_ld32(tmem + lane_off + kColDQ + 32, b);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&sm.dq_consumed);
-            const int ip = qb * kBM + r;
-            if (ip < L) {
-                float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)(start + ip) * P.h_q + h) * kD);
+            // the previous step's reduce must have read the staging buffer
+            if (issuer) bulk_wait_read<0>();
+            named_barrier_sync(1, 128);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    atomicAdd(dst + j, make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                                                   __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3])));
+            for (int half = 0; half < 2; ++half) {
+                uint32_t a[32];
+                tmem_ld32(tmem + lane_off + kColDQ + 32 * half, a);
+                tmem_ld_wait();
+                if (half == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&sm.dq_consumed);
+                }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    atomicAdd(dst + 8 + j, make_float4(__uint_as_float(b[4 * j]), __uint_as_float(b[4 * j + 1]),
-                                                       __uint_as_float(b[4 * j + 2]), __uint_as_float(b[4 * j + 3])));
+                for (int c16 = 0; c16 < 8; ++c16)
+                    *reinterpret_cast<uint4*>(sm.dq_stage[half] + sw128(r, c16 * 16)) =
+                        make_uint4(a[4 * c16], a[4 * c16 + 1], a[4 * c16 + 2], a[4 * c16 + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            named_barrier_sync(1, 128);
+            if (issuer) {
+                // rows past the sequence carry exact zeros (their dS is 0), so adding
+                // them into the next sequence's rows changes nothing
+                tma_reduce_add_3d(&tmDQ, sm.dq_stage[0], 0, h, start + q0);
+                tma_reduce_add_3d(&tmDQ, sm.dq_stage[1], 32, h, start + q0);
+                bulk_commit();
             }
         }
+        if (issuer) bulk_wait_all<0>();
     } else {
         regs_decrease<kCtlRegs>();
         if (warp == 8) {
@@ -268,11 +360,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (lane == 0) {
                 tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
-                tma_prefetch_desc(&tmV);
                 tma_prefetch_desc(&tmDO);
-                mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
-                tma_load_3d(sm.k, &tmK, &sm.kv_full, 0, hk, start + k0);
-                tma_load_3d(sm.v, &tmV, &sm.kv_full, 0, hk, start + k0);
+                mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
+                tma_load_3d(sm.k, &tmK, &sm.k_full, 0, hk, start + k0);
             }
             int issued = 0;
             for (int it = 0; it < nsteps; ++it) {
@@ -291,66 +381,60 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                 for (int u = 0; u < kBM / 32; ++u) {
                     const int c = lane * (kBM / 32) + u;
-                    const int ip = q0 + c;
+                    const int ip = min(q0 + c, L - 1);  // rows past the sequence are masked
                     const size_t ix = (size_t)h * P.total + start + ip;
-                    sm.lse2[st][c] = ip < L ? lse[ix] * kLog2e : INFINITY;
-                    sm.delta[st][c] = ip < L ? delta[ix] : 0.f;
+                    cp_async4(&sm.lse[st][c], lse + ix);
+                    cp_async4(&sm.delta[st][c], delta + ix);
                 }
-                mbar_arrive(&sm.q_full[st]);
+                cp_async_arrive(&sm.q_full[st]);
                 issued = it + 1;
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");
             if (lane == 0) {
-                drain_phase(&sm.kv_full, 0);
+                drain_phase(&sm.k_full, 0);
                 for (int it = max(0, issued - kQStages); it < issued; ++it)
                     drain_phase(&sm.q_full[it % kQStages], (it / kQStages) & 1);
             }
         } else if (warp == 9 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // S^T, dP^T: K-major A and B
-            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);    // dV, dK: B MN-major
-            constexpr uint32_t idQ = idesc_bf16(kBM, kD, 1, 1);    // dQ: A and B MN-major
-            const uint64_t dK_ = smem_desc_sw128(smem_u32(sm.k), 16, 1024);
-            const uint64_t dV_ = smem_desc_sw128(smem_u32(sm.v), 16, 1024);
+            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // S^T, dP^T: A tmem, B K-major
+            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);    // dV, dK: A tmem, B MN-major
+            constexpr uint32_t idQ = idesc_bf16(kBM, kD, 1, 1);    // dQ: A and B MN-major (smem)
             const uint64_t dKmn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
-            bool ok = wait_phase(&sm.kv_full, 0, flags, abort_word) &&
+            bool ok = wait_phase(&sm.kv_tmem, 0, flags, abort_word) &&
+                      wait_phase(&sm.k_full, 0, flags, abort_word) &&
                       wait_phase(&sm.q_full[0], 0, flags, abort_word);
-            auto issue_sdp = [&](int st) {
+            auto issue_s = [&](int st) {  // S^T = K Q^T
                 tc_fence_after();
                 const uint64_t dq_ = smem_desc_sw128(smem_u32(sm.q[st]), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_ts(tmem + kColSdP, tmem + kColK + kk * 8, dq_ + 2 * kk, idSS, kk > 0);
+                mma_commit(&sm.s_full);
+            };
+            auto issue_dp = [&](int st) {  // dP^T = V dO^T
+                tc_fence_after();
                 const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    mma_ss(tmem + kColS, dK_ + 2 * kk, dq_ + 2 * kk, idSS, kk > 0);
-                    mma_ss(tmem + kColDP, dV_ + 2 * kk, ddo + 2 * kk, idSS, kk > 0);
-                }
-                mma_commit(&sm.sdp_full);
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_ts(tmem + kColSdP, tmem + kColV + kk * 8, ddo + 2 * kk, idSS, kk > 0);
+                mma_commit(&sm.dp_full);
             };
-            if (ok) issue_sdp(0);
-            for (int it = 0; ok && it < nsteps; ++it) {
-                const int st = it % kQStages;
-                if (it + 1 < nsteps) {
-                    const int st1 = (it + 1) % kQStages;
-                    if (!(ok = wait_phase(&sm.q_full[st1], ((it + 1) / kQStages) & 1, flags, abort_word)))
-                        break;
-                    if (!(ok = wait_phase(&sm.s_consumed, it & 1, flags, abort_word))) break;
-                    issue_sdp(st1);
-                }
-                if (!(ok = wait_phase(&sm.ds_full, it & 1, flags, abort_word))) break;
+            auto issue_grads = [&](int j) -> bool {
+                const int st = j % kQStages;
+                if (!wait_phase(&sm.ds_full, j & 1, flags, abort_word)) return false;
                 tc_fence_after();
                 const uint64_t ddo_mn = smem_desc_sw128(smem_u32(sm.dout[st]), 1024, 1024);
                 const uint64_t dq_mn = smem_desc_sw128(smem_u32(sm.q[st]), 1024, 1024);
-                const bool acc = it > 0;
 #pragma unroll
                 for (int kk = 0; kk < kBM / 16; ++kk) {
-                    // dV += P^T dO   (A = P^T from tensor memory, K = query rows)
-                    mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + (uint64_t)((kk * 2048) >> 4),
-                           idG, acc || kk > 0);
-                    // dK += dS^T Q   (A = dS^T, K-major: atom kk/4, 32 bytes per 16 rows)
-                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[kk / 4]) + (kk % 4) * 32, 16, 1024);
-                    mma_ss(tmem + kColDK, da, dq_mn + (uint64_t)((kk * 2048) >> 4), idG, acc || kk > 0);
+                    const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
+                    // dV += P^T dO, dK += dS^T Q  (K = query rows)
+                    mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + boff, idG, j > 0 || kk > 0);
+                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG, j > 0 || kk > 0);
                 }
-                if (it > 0) {
-                    if (!(ok = wait_phase(&sm.dq_consumed, (it - 1) & 1, flags, abort_word))) break;
+                if (j > 0) {
+                    if (!wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word)) return false;
                     tc_fence_after();
                 }
 #pragma unroll
@@ -361,7 +445,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 mma_commit(&sm.grads_done);
                 mma_commit(&sm.q_empty[st]);
+                return true;
+            };
+            if (ok) issue_s(0);
+            for (int it = 0; ok && it < nsteps; ++it) {
+                if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
+                issue_dp(it % kQStages);
+                if (it > 0 && !(ok = issue_grads(it - 1))) break;
+                if (it + 1 < nsteps) {
+                    if (!(ok = wait_phase(&sm.q_full[(it + 1) % kQStages], ((it + 1) / kQStages) & 1,
+                                          flags, abort_word)))
+                        break;
+                    if (!(ok = wait_phase(&sm.dp_loaded, it & 1, flags, abort_word))) break;
+                    issue_s((it + 1) % kQStages);
+                }
             }
+            if (ok) issue_grads(nsteps - 1);
             // every MMA issued above must finish before tensor memory is released
             mma_commit(&sm.drained);
             drain_phase(&sm.drained, 0);
@@ -400,11 +499,12 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
                    const float* lse, const float* delta, const void* dout, void* dq, void* dk,
                    void* dv, uint32_t* flags, void* workspace, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
-    CUtensorMap mq, mk, mv, mdo;
+    float* acc = static_cast<float*>(workspace);
+    CUtensorMap mq, mk, mdo, mdq;
     if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM) ||
         !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
-        !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN) ||
-        !make_head_tile_map(&mdo, dout, P.total, P.h_q, kBM))
+        !make_head_tile_map(&mdo, dout, P.total, P.h_q, kBM) ||
+        !make_f32_head_half_map(&mdq, acc, P.total, P.h_q, kBM))
         return cudaErrorInvalidValue;
     // the register split is only safe at exactly this launch value
     cudaFuncAttributes fa;
@@ -414,12 +514,12 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
     const size_t smem = sizeof(BwdSmem) + 1024;
     e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    float* acc = static_cast<float*>(workspace);
     const size_t n = (size_t)P.total * P.h_q * kD;
     e = cudaMemsetAsync(acc, 0, n * sizeof(float), st);
     if (e != cudaSuccess) return e;
     dim3 grid((P.max_seqlen + kBN - 1) / kBN, P.h_kv, P.nseq);
-    bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mv, mdo, P, lse, delta, acc,
+    bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k,
+                                                (const __nv_bfloat16*)v, lse, delta,
                                                 (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, flags);
     count_launches(1);
     e = cudaGetLastError();

@@ -54,4 +54,8 @@ __device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
 // encoder is unavailable or rejects the tensor.
 bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows);
 
+// [T, H, 64] fp32 viewed the same way, box = box_rows tokens x 1 head x 32
+// floats (128 bytes, 128-byte swizzle): used to reduce-add dQ blocks.
+bool make_f32_head_half_map(CUtensorMap* map, void* base, int tokens, int heads, int box_rows);
+
 }  // namespace sinkattn

@@ -377,6 +377,20 @@ bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int head
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T, H, 64] fp32 (the dQ accumulator) as (d, head, token) with 128-byte
+// swizzle; box = box_rows tokens x 1 head x 32 floats (one 128-byte row).
+bool make_f32_head_half_map(CUtensorMap* map, void* base, int tokens, int heads, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)heads * kD * 4};
+    cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_fwd_supported(const Problem& P, bool bf16) {
     return bf16 && P.head_dim == kD && encode_fn() != nullptr && P.total > 0;
 }
