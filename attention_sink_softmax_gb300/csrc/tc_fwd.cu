@@ -176,35 +176,46 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (kp < lo || kp > hi) s[j] = -INFINITY;
                 }
             }
-            float mx8[8];
+            // row max: three-input max, four independent chains
+            float mx4[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx8[u] = s[u];
-#pragma unroll
-            for (int j = 8; j < 128; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
-            const float smax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int j = 8; j < 128; j += 8) {
+                mx4[0] = max3f(mx4[0], s[j], s[j + 1]);
+                mx4[1] = max3f(mx4[1], s[j + 2], s[j + 3]);
+                mx4[2] = max3f(mx4[2], s[j + 4], s[j + 5]);
+                mx4[3] = max3f(mx4[3], s[j + 6], s[j + 7]);
+            }
+            const float smax = max3f(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
             const float mx = smax * sc;
             const bool upd = i == 0 ? mx > m : mx > m + kRescaleLog2;
             const float m_new = upd ? mx : m;
             const float corr = upd ? (m == -INFINITY ? 0.f : fast_exp2(m - m_new)) : 1.f;
             const float mref = m_new == -INFINITY ? 0.f : m_new;
-            float rs8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+            // p = exp2(s * sc - mref), two columns per paired op; row sum in pairs
+            const uint64_t sc2 = f2_pack(sc, sc);
+            const uint64_t nm2 = f2_pack(-mref, -mref);
+            uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int j = 0; j < 64; j += 2) {
-                    const float p0 = fast_exp2(fmaf(s[64 * half + j], sc, -mref));
-                    const float p1 = fast_exp2(fmaf(s[64 * half + j + 1], sc, -mref));
-                    rs8[(j >> 1) & 7] += p0 + p1;
+                    const int c = 64 * half + j;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, nm2), x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
                     pk[j >> 1] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tP + 32 * half, pk);
             }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) +
-                             ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            float r0, r1, r2, r3, r4, r5, r6, r7;
+            f2_unpack(rs2[0], r0, r1);
+            f2_unpack(rs2[1], r2, r3);
+            f2_unpack(rs2[2], r4, r5);
+            f2_unpack(rs2[3], r6, r7);
+            const float rs = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
             if (i > 0 && __any_sync(0xffffffffu, upd)) {
                 uint32_t oa[32], ob[32];
                 tmem_ld32(tO, oa);
