@@ -9,25 +9,23 @@
 // Structure of one CTA: NT query tiles of 128 rows that share a key/value
 // head (NT = 2 query heads of one GQA group when the group size is even), so
 // every K/V tile fetched serves NT tiles.
-//   warp 4*NT      TMA producer: K and V tiles of 128 keys through a
-//                  kStages-deep ring of shared-memory buffers.
-//   warp 4*NT + 1  MMA issuer (one thread): S_t = Q_t K^T (M=128 N=128 K=64)
-//                  then O_t += P_t V (M=128 N=64 K=128), both with the A
-//                  operand read from tensor memory (an MMA with A in tensor
-//                  memory issues about twice as fast as one with A in shared
-//                  memory). Tiles alternate, so one tile's softmax overlaps the
-//                  other tile's MMAs.
+//   warp 4*NT      TMA producer: Q tiles once, then K and V tiles of 128 keys
+//                  through a kStages-deep ring of shared-memory buffers.
+//   warp 4*NT + 1  MMA issuer (one thread): S_t = Q_t K^T (SS, M=128 N=128
+//                  K=64) into tensor memory, then O_t += P_t V (A = P_t read
+//                  from tensor memory, M=128 N=64 K=128). S_t of the next key
+//                  block is issued as soon as the softmax has read S_t into
+//                  registers, so each tile's softmax runs back to back while
+//                  the tensor pipe works on the next block and the other tile.
 //   warps 4t..4t+3 softmax of tile t: thread r owns row r (tensor-memory lane
-//                  r) and first places its row of Q in tensor memory. The running max starts at the sink logit and the running
+//                  r). The running max starts at the sink logit and the running
 //                  sum at the sink's own term, so the sink joins the
 //                  denominator and contributes no value row. The max is only
 //                  moved (and O rescaled in tensor memory) when it grows by
 //                  more than kRescaleLog2 in log2 units; P values then stay
 //                  below 2^kRescaleLog2 and the final O / l is unchanged.
-// Tensor memory (512 columns): S_t at t*128, with P_t (bf16 pairs) written
-// over its first 64 columns once S_t is in registers (the next S_t product is
-// issued after the P_t V product, and products from one thread run in
-// order); O_t at 256 + t*64; Q_t (bf16 pairs) at 384 + t*32. Every mbarrier wait is bounded; a wait that gives up
+// Tensor memory (512 columns): S_t at t*128, O_t at 256 + t*64, P_t (bf16
+// pairs) at 384 + t*64. Every mbarrier wait is bounded; a wait that gives up
 // sets the timeout flag and the CTA winds down without further work.
 #include <cudaTypedefs.h>
 
@@ -63,11 +61,12 @@ constexpr int fwd_threads() { return NT * 128 + 128; }
 
 template <int NT>
 struct FwdSmem {
+    alignas(1024) __nv_bfloat16 q[NT][kBM * kD];
     alignas(1024) __nv_bfloat16 k[kStages][kBN * kD];
     alignas(1024) __nv_bfloat16 v[kStages][kBN * kD];
-    uint64_t q_tmem;
+    uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-    uint64_t s_full[NT], p_full[NT], o_done[NT];
+    uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
     uint64_t drained;
     uint32_t tmem_slot;
     int abort_flag;
@@ -75,8 +74,8 @@ struct FwdSmem {
 
 template <int NT>
 __global__ void __launch_bounds__(fwd_threads<NT>(), 1)
-fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const Problem P, const __nv_bfloat16* __restrict__ qg,
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
               float* __restrict__ lse, uint32_t* flags) {
     extern __shared__ uint8_t smem_raw[];
@@ -101,7 +100,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int hk = h0 / P.group;
 
     if (threadIdx.x == 0) {
-        mbar_init(&sm.q_tmem, NT * 128);
+        mbar_init(&sm.q_full, 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.v_full[i], 1);
@@ -109,6 +108,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         }
         for (int t = 0; t < NT; ++t) {
             mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.s_loaded[t], 128);
             mbar_init(&sm.p_full[t], 128);
             mbar_init(&sm.o_done[t], 1);
         }
@@ -135,35 +135,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * 128;
         const uint32_t tO = tmem + lane_off + 256 + t * 64;
-        const uint32_t tP = tS;  // P overwrites the first half of S once S is in registers
-        {
-            // A operand of S = Q K^T: this row's Q (zeros past the sequence)
-            uint32_t qrow[32];
-            const uint4* src = reinterpret_cast<const uint4*>(qg + ((size_t)(start + row) * P.h_q + h) * kD);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 x = valid ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
-                qrow[4 * j] = x.x;
-                qrow[4 * j + 1] = x.y;
-                qrow[4 * j + 2] = x.z;
-                qrow[4 * j + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + 384 + t * 32, qrow);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&sm.q_tmem);
-        }
+        const uint32_t tP = tmem + lane_off + 384 + t * 64;
         const float sc = P.scale_log2;
         float m = __ldg(sinks + h) * kLog2e;  // running max in log2 units, seeded by the sink
         float l = m == -INFINITY ? 0.f : 1.f;  // running sum, seeded by the sink's own term
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
             ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], i & 1, flags, abort_word));
-            // S_t(i) was committed after PV(t, i-1), so that product has finished
-            // too: O_t and P_t are free to touch
-            if (ok && i > 0)
-                ok = __all_sync(0xffffffffu,
-                                wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word));
             if (!ok) break;
             tc_fence_after();
             float s[128];
@@ -174,6 +152,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 tmem_ld32(tS + 64, c);
                 tmem_ld32(tS + 96, d);
                 tmem_ld_wait();
+                // S_t is in registers: the next block's S_t product may be issued
+                tc_fence_before();
+                mbar_arrive(&sm.s_loaded[t]);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     s[j] = __uint_as_float(a[j]);
@@ -215,6 +196,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             const uint64_t sc2 = f2_pack(sc, sc);
             const uint64_t nm2 = f2_pack(-mref, -mref);
             uint64_t rs2[4] = {0, 0, 0, 0};
+            // P_t and O_t are read by the previous block's P V product: wait for it
+            if (i > 0) {
+                ok = __all_sync(0xffffffffu,
+                                wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word));
+                if (!ok) break;
+                tc_fence_after();
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
@@ -293,8 +281,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         if (warp == 4 * NT) {
             // ------------------------------------------------------------ TMA producer
             if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
+                mbar_arrive_expect_tx(&sm.q_full, NT * kTileBytes);
+                for (int t = 0; t < NT; ++t) tma_load_3d(sm.q[t], &tmQ, &sm.q_full, 0, h0 + t, start + r0);
                 int issued = 0;
                 for (int i = 0; i < nblk; ++i) {
                     const int st = i % kStages;
@@ -309,6 +300,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                     issued = i + 1;
                 }
                 // copies still in flight must land before the CTA's shared memory goes away
+                drain_phase(&sm.q_full, 0);
                 for (int i = max(0, issued - kStages); i < issued; ++i) {
                     const int st = i % kStages;
                     drain_phase(&sm.k_full[st], (i / kStages) & 1);
@@ -318,43 +310,47 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         } else if (warp == 4 * NT + 1) {
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
-                constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q from TMEM, K K-major
+                constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q, K both K-major
                 constexpr uint32_t idO = idesc_bf16(kBM, kD, 0, 1);   // P from TMEM, V MN-major
-                bool ok = wait_phase(&sm.q_tmem, 0, flags, abort_word) &&
+                uint64_t dq[NT];
+                for (int t = 0; t < NT; ++t) dq[t] = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
+                bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
                           wait_phase(&sm.k_full[0], 0, flags, abort_word);
                 if (ok) {
                     tc_fence_after();
                     const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
                     for (int t = 0; t < NT; ++t) {
                         for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_ts(tmem + t * 128, tmem + 384 + t * 32 + kk * 8, dk + 2 * kk, idS, kk > 0);
+                            mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
                         mma_commit(&sm.s_full[t]);
                     }
                 }
                 for (int i = 0; ok && i < nblk; ++i) {
                     const int st = i % kStages;
-                    if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
+                    const int st1 = (i + 1) % kStages;
                     const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
                     for (int t = 0; t < NT; ++t) {
-                        if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
-                        tc_fence_after();
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tmem + 256 + t * 64, tmem + t * 128 + kk * 8,
-                                   dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
-                        mma_commit(&sm.o_done[t]);
                         if (i + 1 < nblk) {
-                            const int st1 = (i + 1) % kStages;
-                            if (t == 0) {
-                                if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags,
-                                                      abort_word)))
-                                    break;
-                                tc_fence_after();
-                            }
+                            // S_t(i+1) = Q_t K(i+1)^T as soon as S_t(i) has been read
+                            if (!(ok = wait_phase(&sm.s_loaded[t], i & 1, flags, abort_word))) break;
+                            if (t == 0 &&
+                                !(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word)))
+                                break;
+                            tc_fence_after();
                             const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st1]), 16, 1024);
                             for (int kk = 0; kk < kD / 16; ++kk)
-                                mma_ts(tmem + t * 128, tmem + 384 + t * 32 + kk * 8, dk + 2 * kk, idS, kk > 0);
+                                mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
                             mma_commit(&sm.s_full[t]);
                         }
+                        // O_t += P_t(i) V(i)
+                        if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
+                        if (t == 0 && !(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word)))
+                            break;
+                        tc_fence_after();
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8,
+                                   dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
+                        mma_commit(&sm.o_done[t]);
                     }
                     mma_commit(&sm.kv_empty[st]);
                 }
@@ -423,7 +419,7 @@ bool tc_fwd_supported(const Problem& P, bool bf16) {
 size_t tc_fwd_workspace_bytes(const Problem&, bool) { return 0; }
 
 template <int NT>
-static cudaError_t launch_fwd(const Problem& P, const void* q, const CUtensorMap& mk,
+static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const float* sinks, void* o, float* lse,
                               uint32_t* flags, cudaStream_t st) {
     if (NT == 2) {
@@ -438,8 +434,8 @@ static cudaError_t launch_fwd(const Problem& P, const void* q, const CUtensorMap
         fwd_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid((P.max_seqlen + kBM - 1) / kBM, P.h_q / NT, P.nseq);
-    fwd_tc_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mk, mv, P, (const __nv_bfloat16*)q,
-                                                             sinks, (__nv_bfloat16*)o, lse, flags);
+    fwd_tc_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
+                                                         (__nv_bfloat16*)o, lse, flags);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -448,12 +444,13 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
                    const float* sinks, void* o, float* lse, uint32_t* flags, void*,
                    cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
-    CUtensorMap mk, mv;
-    if (!make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
+    CUtensorMap mq, mk, mv;
+    if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM) ||
+        !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
         !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN))
         return cudaErrorInvalidValue;
-    if (P.group % 2 == 0) return launch_fwd<2>(P, q, mk, mv, sinks, o, lse, flags, st);
-    return launch_fwd<1>(P, q, mk, mv, sinks, o, lse, flags, st);
+    if (P.group % 2 == 0) return launch_fwd<2>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    return launch_fwd<1>(P, mq, mk, mv, sinks, o, lse, flags, st);
 }
 
 }  // namespace sinkattn
