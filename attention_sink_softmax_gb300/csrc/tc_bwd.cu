@@ -27,7 +27,9 @@
 // into registers, then dP^T is computed into the same columns while they
 // exponentiate. Per step the tensor pipe runs dP(i), the gradients of step
 // i-1, then S(i+1), so the elementwise work of step i overlaps the gradient
-// products of step i-1.
+// products of step i-1. The P^T / dS^T columns are released as soon as dV and
+// dK of step i-1 are done, and dS goes to one of two shared-memory buffers, so
+// step i's stores never wait for the dQ product of step i-1.
 //
 // Warps: 0-7 elementwise (thread = key = tensor-memory lane; warpgroup w takes
 // query rows [64w, 64w+64) of the step); 8 producer (TMA for K, Q, dO and
@@ -73,15 +75,17 @@ struct BwdSmem {
     alignas(1024) __nv_bfloat16 k[kBN * kD];  // B operand of dQ
     alignas(1024) __nv_bfloat16 q[kQStages][kBM * kD];
     alignas(1024) __nv_bfloat16 dout[kQStages][kBM * kD];
-    // dS: two 16 KB atoms (query rows 0..63 and 64..127), each 128 keys x 128 bytes
-    alignas(1024) uint8_t ds[2][kBN * 128];
+    // dS, double-buffered by step parity: two 16 KB atoms (query rows 0..63 and
+    // 64..127), each 128 keys x 128 bytes
+    alignas(1024) uint8_t ds[2][2][kBN * 128];
     // dQ block staged for the bulk reduce: columns 0..31 and 32..63, 128 rows x 128 bytes
     alignas(1024) uint8_t dq_stage[2][kBM * 128];
     alignas(16) float lse[kQStages][kBM];  // rows past the sequence hold a clamped copy
     alignas(16) float delta[kQStages][kBM];
     uint64_t k_full, kv_tmem;
     uint64_t q_full[kQStages], q_empty[kQStages];
-    uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, grads_done, dq_consumed, drained;
+    uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, pd_free, ds_free[2], grads_done,
+        dq_consumed, acc_done, drained;
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -151,8 +155,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(&sm.dp_full, 1);
         mbar_init(&sm.dp_loaded, 256);
         mbar_init(&sm.ds_full, 256);
+        mbar_init(&sm.pd_free, 1);
+        mbar_init(&sm.ds_free[0], 1);
+        mbar_init(&sm.ds_free[1], 1);
         mbar_init(&sm.grads_done, 1);
         mbar_init(&sm.dq_consumed, 128);
+        mbar_init(&sm.acc_done, 1);
         mbar_init(&sm.drained, 1);
         sm.abort_flag = 0;
         fence_barrier_init();
@@ -270,17 +278,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // dP^T has been read: the next step's S^T may overwrite the columns
             tc_fence_before();
             mbar_arrive(&sm.dp_loaded);
-            // the previous step's gradient products read P^T, dS^T and dS: wait for them
+            // P^T and dS^T are read by the previous step's dV and dK products, and
+            // this step's dS buffer by the dQ product of two steps back: wait for them
             if (it > 0) {
-                ok = __all_sync(0xffffffffu,
-                                wait_phase(&sm.grads_done, (it - 1) & 1, flags, abort_word));
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.pd_free, (it - 1) & 1, flags, abort_word));
+                if (!ok) break;
+            }
+            if (it > 1) {
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1,
+                                                        flags, abort_word));
                 if (!ok) break;
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
             tmem_st32(tmem + lane_off + kColDS + 32 * w, pd);
             // dS row of this key: 64 query rows = 128 bytes of atom w (A operand of dQ)
-            uint8_t* atom = sm.ds[w];
+            uint8_t* atom = sm.ds[it & 1][w];
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) {
                 const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
@@ -291,10 +304,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_before();
             mbar_arrive(&sm.ds_full);
         }
-        // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled)
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            wait_phase(&sm.grads_done, (nsteps - 1) & 1, flags, abort_word));
+        // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled). These
+        // warps do not wait on every phase of grads_done, so a parity wait on it
+        // could match a phase two steps back: the single-phase acc_done is used.
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.acc_done, 0, flags, abort_word));
         if (ok) {
             tc_fence_after();
             uint32_t a[32], b[32];
@@ -433,6 +446,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + boff, idG, j > 0 || kk > 0);
                     mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG, j > 0 || kk > 0);
                 }
+                mma_commit(&sm.pd_free);
                 if (j > 0) {
                     if (!wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word)) return false;
                     tc_fence_after();
@@ -440,9 +454,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     // dQ = dS K   (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
-                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[0]) + kk * 2048, kBN * 128, 1024);
+                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[j & 1][0]) + kk * 2048, kBN * 128, 1024);
                     mma_ss(tmem + kColDQ, da, dKmn + (uint64_t)((kk * 2048) >> 4), idQ, kk > 0);
                 }
+                mma_commit(&sm.ds_free[j & 1]);
                 mma_commit(&sm.grads_done);
                 mma_commit(&sm.q_empty[st]);
                 return true;
@@ -460,7 +475,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     issue_s((it + 1) % kQStages);
                 }
             }
-            if (ok) issue_grads(nsteps - 1);
+            if (ok && issue_grads(nsteps - 1)) mma_commit(&sm.acc_done);
             // every MMA issued above must finish before tensor memory is released
             mma_commit(&sm.drained);
             drain_phase(&sm.drained, 0);
