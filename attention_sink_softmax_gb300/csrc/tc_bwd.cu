@@ -25,18 +25,21 @@
 //   dQ   = dS K      A = dS   (smem: needs query rows as M)   B = K  (smem)
 // S^T and dP^T share one 128-column region: the elementwise warps read S^T
 // into registers, then dP^T is computed into the same columns while they
-// exponentiate. Per step the tensor pipe runs dP(i), the gradients of step
-// i-1, then S(i+1), so the elementwise work of step i overlaps the gradient
-// products of step i-1. The P^T / dS^T columns are released as soon as dV and
-// dK of step i-1 are done, and dS goes to one of two shared-memory buffers, so
-// step i's stores never wait for the dQ product of step i-1.
+// exponentiate. Two threads issue MMAs: one issues S^T and dP^T, the other
+// dV, dK and dQ, so the tensor pipe always has one stream's products queued
+// while the other thread waits on a barrier. The elementwise work of step i
+// overlaps the gradient products of step i-1. The P^T / dS^T columns are
+// released as soon as dV and dK of step i-1 are done, and dS goes to one of
+// two shared-memory buffers, so step i's stores never wait for the dQ product
+// of step i-1. A Q / dO stage is refilled once both issuers are done with it.
 //
 // Warps: 0-7 elementwise (thread = key = tensor-memory lane; warpgroup w takes
 // query rows [64w, 64w+64) of the step); 8 producer (TMA for K, Q, dO and
-// cp.async for the step's LSE and delta rows, through a kQStages ring); 9 MMA
-// issuer (one thread); 12-15 dQ drain (tensor memory -> shared staging -> TMA
-// bulk reduce-add). Tensor memory: S^T/dP^T 0..127, dV 128..191, dK
-// 192..255, dQ 256..319, K 320..351, V 352..383, P^T 384..447, dS^T 448..511.
+// cp.async for the step's LSE and delta rows, through a kQStages ring); 9 and
+// 10 MMA issuers (one thread each); 12-15 dQ drain (tensor memory -> shared
+// staging -> TMA bulk reduce-add). Tensor memory: S^T/dP^T 0..127, dV
+// 128..191, dK 192..255, dQ 256..319, K 320..351, V 352..383, P^T 384..447,
+// dS^T 448..511.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -85,7 +88,7 @@ struct BwdSmem {
     uint64_t k_full, kv_tmem;
     uint64_t q_full[kQStages], q_empty[kQStages];
     uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, pd_free, ds_free[2], grads_done,
-        dq_consumed, acc_done, drained;
+        dq_consumed, acc_done, drained[2];
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -148,7 +151,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(&sm.kv_tmem, 256);
         for (int i = 0; i < kQStages; ++i) {
             mbar_init(&sm.q_full[i], 1 + 32);
-            mbar_init(&sm.q_empty[i], 1);
+            mbar_init(&sm.q_empty[i], 2);  // one commit from each MMA issuer
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.s_loaded, 256);
@@ -161,7 +164,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(&sm.grads_done, 1);
         mbar_init(&sm.dq_consumed, 128);
         mbar_init(&sm.acc_done, 1);
-        mbar_init(&sm.drained, 1);
+        mbar_init(&sm.drained[0], 1);
+        mbar_init(&sm.drained[1], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
     }
@@ -409,13 +413,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     drain_phase(&sm.q_full[it % kQStages], (it / kQStages) & 1);
             }
         } else if (warp == 9 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // S^T, dP^T: A tmem, B K-major
-            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);    // dV, dK: A tmem, B MN-major
-            constexpr uint32_t idQ = idesc_bf16(kBM, kD, 1, 1);    // dQ: A and B MN-major (smem)
-            const uint64_t dKmn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
+            // -------------------------------------------------------- MMA issuer 1: S^T, dP^T
+            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // A tmem, B K-major
             bool ok = wait_phase(&sm.kv_tmem, 0, flags, abort_word) &&
-                      wait_phase(&sm.k_full, 0, flags, abort_word) &&
                       wait_phase(&sm.q_full[0], 0, flags, abort_word);
             auto issue_s = [&](int st) {  // S^T = K Q^T
                 tc_fence_after();
@@ -425,48 +425,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     mma_ts(tmem + kColSdP, tmem + kColK + kk * 8, dq_ + 2 * kk, idSS, kk > 0);
                 mma_commit(&sm.s_full);
             };
-            auto issue_dp = [&](int st) {  // dP^T = V dO^T
+            if (ok) issue_s(0);
+            for (int it = 0; ok && it < nsteps; ++it) {
+                const int st = it % kQStages;
+                if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
+                // dP^T = V dO^T into the columns S^T was read from
                 tc_fence_after();
                 const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     mma_ts(tmem + kColSdP, tmem + kColV + kk * 8, ddo + 2 * kk, idSS, kk > 0);
                 mma_commit(&sm.dp_full);
-            };
-            auto issue_grads = [&](int j) -> bool {
-                const int st = j % kQStages;
-                if (!wait_phase(&sm.ds_full, j & 1, flags, abort_word)) return false;
-                tc_fence_after();
-                const uint64_t ddo_mn = smem_desc_sw128(smem_u32(sm.dout[st]), 1024, 1024);
-                const uint64_t dq_mn = smem_desc_sw128(smem_u32(sm.q[st]), 1024, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kBM / 16; ++kk) {
-                    const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
-                    // dV += P^T dO, dK += dS^T Q  (K = query rows)
-                    mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + boff, idG, j > 0 || kk > 0);
-                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG, j > 0 || kk > 0);
-                }
-                mma_commit(&sm.pd_free);
-                if (j > 0) {
-                    if (!wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word)) return false;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // dQ = dS K   (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
-                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[j & 1][0]) + kk * 2048, kBN * 128, 1024);
-                    mma_ss(tmem + kColDQ, da, dKmn + (uint64_t)((kk * 2048) >> 4), idQ, kk > 0);
-                }
-                mma_commit(&sm.ds_free[j & 1]);
-                mma_commit(&sm.grads_done);
-                mma_commit(&sm.q_empty[st]);
-                return true;
-            };
-            if (ok) issue_s(0);
-            for (int it = 0; ok && it < nsteps; ++it) {
-                if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
-                issue_dp(it % kQStages);
-                if (it > 0 && !(ok = issue_grads(it - 1))) break;
+                mma_commit(&sm.q_empty[st]);  // this issuer's last read of the step's Q / dO stage
                 if (it + 1 < nsteps) {
                     if (!(ok = wait_phase(&sm.q_full[(it + 1) % kQStages], ((it + 1) / kQStages) & 1,
                                           flags, abort_word)))
@@ -475,10 +445,47 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     issue_s((it + 1) % kQStages);
                 }
             }
-            if (ok && issue_grads(nsteps - 1)) mma_commit(&sm.acc_done);
             // every MMA issued above must finish before tensor memory is released
-            mma_commit(&sm.drained);
-            drain_phase(&sm.drained, 0);
+            mma_commit(&sm.drained[0]);
+            drain_phase(&sm.drained[0], 0);
+        } else if (warp == 10 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer 2: dV, dK, dQ
+            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);  // dV, dK: A tmem, B MN-major
+            constexpr uint32_t idQ = idesc_bf16(kBM, kD, 1, 1);  // dQ: A and B MN-major (smem)
+            const uint64_t dKmn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
+            bool ok = wait_phase(&sm.k_full, 0, flags, abort_word);
+            for (int j = 0; ok && j < nsteps; ++j) {
+                const int st = j % kQStages;
+                // dV += P^T dO, dK += dS^T Q  (K = query rows)
+                if (!(ok = wait_phase(&sm.ds_full, j & 1, flags, abort_word))) break;
+                tc_fence_after();
+                const uint64_t ddo_mn = smem_desc_sw128(smem_u32(sm.dout[st]), 1024, 1024);
+                const uint64_t dq_mn = smem_desc_sw128(smem_u32(sm.q[st]), 1024, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBM / 16; ++kk) {
+                    const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
+                    mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + boff, idG, j > 0 || kk > 0);
+                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG, j > 0 || kk > 0);
+                }
+                // P^T, dS^T and the step's Q / dO stage are no longer read
+                mma_commit(&sm.pd_free);
+                mma_commit(&sm.q_empty[st]);
+                // dQ = dS K  (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
+                if (j > 0) {
+                    if (!(ok = wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word))) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[j & 1][0]) + kk * 2048, kBN * 128, 1024);
+                    mma_ss(tmem + kColDQ, da, dKmn + (uint64_t)((kk * 2048) >> 4), idQ, kk > 0);
+                }
+                mma_commit(&sm.ds_free[j & 1]);
+                mma_commit(&sm.grads_done);
+            }
+            if (ok) mma_commit(&sm.acc_done);
+            mma_commit(&sm.drained[1]);
+            drain_phase(&sm.drained[1], 0);
         }
     }
     tc_fence_before();
