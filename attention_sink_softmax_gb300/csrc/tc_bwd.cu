@@ -204,10 +204,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_arrive(&sm.kv_tmem);
         }
         bool ok = true;
+        bool s_ready = false;  // S^T of this step seen complete by an early poll
         for (int it = 0; it < nsteps; ++it) {
             const int st = it % kQStages;
             const int q0 = (qb_lo + it % nq) * kBM;
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, it & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, s_ready || wait_phase(&sm.s_full, it & 1, flags, abort_word));
             if (!ok) break;
             tc_fence_after();
             float p[64];  // P^T for this key and query rows [64w, 64w+64)
@@ -258,40 +259,45 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, it & 1, flags, abort_word));
             if (!ok) break;
             tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                uint32_t d[32];
-                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32 * ch, d);
+            {
+                uint32_t d0[32], d1[32];
+                tmem_ld32(tmem + lane_off + kColSdP + 64 * w, d0);
+                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32, d1);
+                // P^T and dS^T are read by the previous step's dV and dK products, and
+                // this step's dS buffer by the dQ product of two steps back: poll their
+                // barriers now, while the loads are in flight, and wait below if needed
+                const bool pd_ready = it == 0 || mbar_test_wait(&sm.pd_free, (it - 1) & 1);
+                const bool ds_ready = it <= 1 || mbar_test_wait(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
+                for (int j = 0; j < 64; j += 4) {
                     // dS = P (dP - delta), two columns per paired op
-                    const float4 D4 = *reinterpret_cast<const float4*>(&sm.delta[st][64 * w + 32 * ch + j]);
-                    const int c = 32 * ch + j;
-                    const uint64_t t01 = f2_sub(f2_pack(__uint_as_float(d[j]), __uint_as_float(d[j + 1])),
+                    const float4 D4 = *reinterpret_cast<const float4*>(&sm.delta[st][64 * w + j]);
+                    const uint32_t* d = j < 32 ? d0 + j : d1 + (j - 32);
+                    const uint64_t t01 = f2_sub(f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1])),
                                                 f2_pack(D4.x, D4.y));
-                    const uint64_t t23 = f2_sub(f2_pack(__uint_as_float(d[j + 2]), __uint_as_float(d[j + 3])),
+                    const uint64_t t23 = f2_sub(f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3])),
                                                 f2_pack(D4.z, D4.w));
                     float y0, y1, y2, y3;
-                    f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t01), y0, y1);
-                    f2_unpack(f2_mul(f2_pack(p[c + 2], p[c + 3]), t23), y2, y3);
-                    pd[16 * ch + j / 2] = pack_bf16x2(y0, y1);
-                    pd[16 * ch + j / 2 + 1] = pack_bf16x2(y2, y3);
+                    f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t01), y0, y1);
+                    f2_unpack(f2_mul(f2_pack(p[j + 2], p[j + 3]), t23), y2, y3);
+                    pd[j / 2] = pack_bf16x2(y0, y1);
+                    pd[j / 2 + 1] = pack_bf16x2(y2, y3);
                 }
-            }
-            // dP^T has been read: the next step's S^T may overwrite the columns
-            tc_fence_before();
-            mbar_arrive(&sm.dp_loaded);
-            // P^T and dS^T are read by the previous step's dV and dK products, and
-            // this step's dS buffer by the dQ product of two steps back: wait for them
-            if (it > 0) {
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.pd_free, (it - 1) & 1, flags, abort_word));
-                if (!ok) break;
-            }
-            if (it > 1) {
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1,
-                                                        flags, abort_word));
-                if (!ok) break;
+                // dP^T has been read: the next step's S^T may overwrite the columns
+                tc_fence_before();
+                mbar_arrive(&sm.dp_loaded);
+                if (it > 0) {
+                    ok = __all_sync(0xffffffffu, pd_ready || wait_phase(&sm.pd_free, (it - 1) & 1, flags,
+                                                                        abort_word));
+                    if (!ok) break;
+                }
+                if (it > 1) {
+                    ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
+                                                                        ((it >> 1) - 1) & 1, flags,
+                                                                        abort_word));
+                    if (!ok) break;
+                }
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
@@ -304,6 +310,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // poll the next step's S^T while the stores drain
+            s_ready = it + 1 < nsteps && mbar_test_wait(&sm.s_full, (it + 1) & 1);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.ds_full);
@@ -428,6 +436,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (ok) issue_s(0);
             for (int it = 0; ok && it < nsteps; ++it) {
                 const int st = it % kQStages;
+                const int st1 = (it + 1) % kQStages;
+                // early poll of the next step's Q / dO stage (answer used after dP)
+                const bool q_ready = it + 1 >= nsteps || mbar_test_wait(&sm.q_full[st1], ((it + 1) / kQStages) & 1);
                 if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
                 // dP^T = V dO^T into the columns S^T was read from
                 tc_fence_after();
@@ -438,11 +449,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mma_commit(&sm.dp_full);
                 mma_commit(&sm.q_empty[st]);  // this issuer's last read of the step's Q / dO stage
                 if (it + 1 < nsteps) {
-                    if (!(ok = wait_phase(&sm.q_full[(it + 1) % kQStages], ((it + 1) / kQStages) & 1,
-                                          flags, abort_word)))
+                    if (!(ok = q_ready || wait_phase(&sm.q_full[st1], ((it + 1) / kQStages) & 1, flags,
+                                                     abort_word)))
                         break;
                     if (!(ok = wait_phase(&sm.dp_loaded, it & 1, flags, abort_word))) break;
-                    issue_s((it + 1) % kQStages);
+                    issue_s(st1);
                 }
             }
             // every MMA issued above must finish before tensor memory is released
