@@ -11,12 +11,15 @@
 // every K/V tile fetched serves NT tiles.
 //   warp 4*NT      TMA producer: Q tiles once, then K and V tiles of 128 keys
 //                  through a kStages-deep ring of shared-memory buffers.
-//   warp 4*NT + 1  MMA issuer (one thread): S_t = Q_t K^T (SS, M=128 N=128
-//                  K=64) into tensor memory, then O_t += P_t V (A = P_t read
-//                  from tensor memory, M=128 N=64 K=128). S_t of the next key
-//                  block is issued as soon as the softmax has read S_t into
-//                  registers, so each tile's softmax runs back to back while
-//                  the tensor pipe works on the next block and the other tile.
+//   warp 4*NT+1+t  MMA issuer of tile t (one thread): S_t = Q_t K^T (SS, M=128
+//                  N=128 K=64) into tensor memory, then O_t += P_t V (A = P_t
+//                  read from tensor memory, M=128 N=64 K=128). S_t of the next
+//                  key block is issued as soon as the softmax has read S_t
+//                  into registers, so each tile's softmax runs back to back
+//                  while the tensor pipe works on the next block and the other
+//                  tile. One issuer per tile keeps a wait on one tile from
+//                  holding back the other tile's products; a K/V stage is
+//                  refilled once every tile's issuer is done with it.
 //   warps 4t..4t+3 softmax of tile t: thread r owns row r (tensor-memory lane
 //                  r). The running max starts at the sink logit and the running
 //                  sum at the sink's own term, so the sink joins the
@@ -67,7 +70,7 @@ struct FwdSmem {
     uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
-    uint64_t drained;
+    uint64_t drained[NT];
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -104,7 +107,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.v_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+            mbar_init(&sm.kv_empty[i], NT);  // one commit from each tile's MMA issuer
         }
         for (int t = 0; t < NT; ++t) {
             mbar_init(&sm.s_full[t], 1);
@@ -112,7 +115,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&sm.p_full[t], 128);
             mbar_init(&sm.o_done[t], 1);
         }
-        mbar_init(&sm.drained, 1);
+        for (int t = 0; t < NT; ++t) mbar_init(&sm.drained[t], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
     }
@@ -307,57 +310,48 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     drain_phase(&sm.v_full[st], (i / kStages) & 1);
                 }
             }
-        } else if (warp == 4 * NT + 1) {
-            // ------------------------------------------------------------ MMA issuer
-            if (lane == 0) {
-                constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q, K both K-major
-                constexpr uint32_t idO = idesc_bf16(kBM, kD, 0, 1);   // P from TMEM, V MN-major
-                uint64_t dq[NT];
-                for (int t = 0; t < NT; ++t) dq[t] = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
-                bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
-                          wait_phase(&sm.k_full[0], 0, flags, abort_word);
-                if (ok) {
-                    tc_fence_after();
-                    const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
-                    for (int t = 0; t < NT; ++t) {
-                        for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
-                        mma_commit(&sm.s_full[t]);
-                    }
-                }
-                for (int i = 0; ok && i < nblk; ++i) {
-                    const int st = i % kStages;
-                    const int st1 = (i + 1) % kStages;
-                    const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
-                    for (int t = 0; t < NT; ++t) {
-                        if (i + 1 < nblk) {
-                            // S_t(i+1) = Q_t K(i+1)^T as soon as S_t(i) has been read
-                            if (!(ok = wait_phase(&sm.s_loaded[t], i & 1, flags, abort_word))) break;
-                            if (t == 0 &&
-                                !(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word)))
-                                break;
-                            tc_fence_after();
-                            const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st1]), 16, 1024);
-                            for (int kk = 0; kk < kD / 16; ++kk)
-                                mma_ss(tmem + t * 128, dq[t] + 2 * kk, dk + 2 * kk, idS, kk > 0);
-                            mma_commit(&sm.s_full[t]);
-                        }
-                        // O_t += P_t(i) V(i)
-                        if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
-                        if (t == 0 && !(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word)))
-                            break;
-                        tc_fence_after();
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tmem + 256 + t * 64, tmem + 384 + t * 64 + kk * 8,
-                                   dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
-                        mma_commit(&sm.o_done[t]);
-                    }
-                    mma_commit(&sm.kv_empty[st]);
-                }
-                // every MMA issued above must finish before tensor memory is released
-                mma_commit(&sm.drained);
-                drain_phase(&sm.drained, 0);
+        } else if (warp >= 4 * NT + 1 && warp <= 4 * NT + NT && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer of tile t
+            const int t = warp - (4 * NT + 1);
+            constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q, K both K-major
+            constexpr uint32_t idO = idesc_bf16(kBM, kD, 0, 1);   // P from TMEM, V MN-major
+            const uint64_t dq = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
+            const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
+            bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
+                      wait_phase(&sm.k_full[0], 0, flags, abort_word);
+            if (ok) {
+                tc_fence_after();
+                const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+                for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                mma_commit(&sm.s_full[t]);
             }
+            for (int i = 0; ok && i < nblk; ++i) {
+                const int st = i % kStages;
+                const int st1 = (i + 1) % kStages;
+                if (i + 1 < nblk) {
+                    // S_t(i+1) = Q_t K(i+1)^T as soon as S_t(i) has been read
+                    if (!(ok = wait_phase(&sm.s_loaded[t], i & 1, flags, abort_word))) break;
+                    if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word)))
+                        break;
+                    tc_fence_after();
+                    const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st1]), 16, 1024);
+                    for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                    mma_commit(&sm.s_full[t]);
+                }
+                // O_t += P_t(i) V(i)
+                if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
+                tc_fence_after();
+                const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tO, tP + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
+                mma_commit(&sm.o_done[t]);
+                // this tile's last reads of stage st (K(i) by S_t(i), V(i) by the product above)
+                mma_commit(&sm.kv_empty[st]);
+            }
+            // every MMA issued above must finish before tensor memory is released
+            mma_commit(&sm.drained[t]);
+            drain_phase(&sm.drained[t], 0);
         }
     }
     tc_fence_before();
