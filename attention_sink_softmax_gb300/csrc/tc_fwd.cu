@@ -70,6 +70,7 @@ struct FwdSmem {
     uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
+    uint64_t exp_turn[NT];  // the two tiles' exponentials take turns (NT = 2)
     uint64_t drained[NT];
     uint32_t tmem_slot;
     int abort_flag;
@@ -114,6 +115,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&sm.s_loaded[t], 128);
             mbar_init(&sm.p_full[t], 128);
             mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.exp_turn[t], 128);
         }
         for (int t = 0; t < NT; ++t) mbar_init(&sm.drained[t], 1);
         sm.abort_flag = 0;
@@ -199,28 +201,37 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const uint64_t sc2 = f2_pack(sc, sc);
             const uint64_t nm2 = f2_pack(-mref, -mref);
             uint64_t rs2[4] = {0, 0, 0, 0};
-            // P_t and O_t are read by the previous block's P V product: wait for it
+            // With two tiles the exponentials alternate (tile 0 block i, tile 1 block
+            // i, tile 0 block i+1, ...), so one tile's exp2 loop overlaps the other
+            // tile's loads, max and stores instead of both competing for the
+            // special-function units at once.
+            if (NT == 2 && (t == 1 || i > 0)) {
+                const int ph = t == 0 ? i - 1 : i;
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word));
+                if (!ok) break;
+            }
+            // P into registers first (bf16 pairs): the exponentials overlap the
+            // previous block's P V product, which still reads P_t and writes O_t
+            uint32_t pk0[32], pk1[32];
+#pragma unroll
+            for (int j = 0; j < 128; j += 2) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[j], s[j + 1]), sc2, nm2), x0, x1);
+                const float p0 = fast_exp2(x0);
+                const float p1 = fast_exp2(x1);
+                rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
+                if (j < 64) pk0[j >> 1] = pack_bf16x2(p0, p1);
+                else pk1[(j - 64) >> 1] = pack_bf16x2(p0, p1);
+            }
+            if (NT == 2) mbar_arrive(&sm.exp_turn[(1 - t) % NT]);
             if (i > 0) {
                 ok = __all_sync(0xffffffffu,
                                 wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word));
                 if (!ok) break;
                 tc_fence_after();
             }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    const int c = 64 * half + j;
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, nm2), x0, x1);
-                    const float p0 = fast_exp2(x0);
-                    const float p1 = fast_exp2(x1);
-                    rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
-                    pk[j >> 1] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tP + 32 * half, pk);
-            }
+            tmem_st32(tP, pk0);
+            tmem_st32(tP + 32, pk1);
             float r0, r1, r2, r3, r4, r5, r6, r7;
             f2_unpack(rs2[0], r0, r1);
             f2_unpack(rs2[1], r2, r3);
