@@ -132,6 +132,39 @@ def dist_env():
     return ws, rank, local
 
 
+def init_dist(ws: int, backend: str) -> None:
+    """One process per GPU (torchrun); ``backend`` is nccl on GPUs, gloo in tests."""
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend)
+
+
+def rank_seed(w: inputs.Workload, rank: int) -> int:
+    """Each replica draws its own batch (weak scaling: per-GPU work is fixed)."""
+    return w.seed + rank
+
+
+def aggregate_value(flops_per_rank_step: float, ws: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_rank_step * ws / (ms_max / 1000) / 1e12
+
+
+def emit(line: dict, rank: int) -> str | None:
+    """Rank 0 alone prints the JSON line; returns what was printed."""
+    if rank != 0:
+        return None
+    text = json.dumps(line)
+    print(text, flush=True)
+    return text
+
+
+def config_of(w: inputs.Workload, window: int, ws: int) -> dict:
+    return {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen, "h_q": w.h_q,
+            "h_kv": w.h_kv, "head_dim": w.head_dim, "causal": w.causal,
+            "window": window, "tokens": w.total_tokens,
+            "flops_per_step": sum(flops_of(w, window)), "l2": "inputs exceed L2 (no flush)",
+            "parallelism": f"replicas x{ws} (independent batches, no collective)"}
+
+
 def barrier(ws):
     if ws > 1:
         torch.distributed.barrier()
@@ -222,12 +255,12 @@ def run_reference(args, w, window):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "sample": info["sample"]},
+        "data": "synthetic", "config": config_of(w, window, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"],
                          "kind": "oracle", "sample": info["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line, rank)
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -265,7 +298,7 @@ def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, ls
     torch.cuda.synchronize(dev)
     barrier(ws)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    e2e_value = flops_step * ws / (ms_e2e / 1000) / 1e12
+    e2e_value = aggregate_value(flops_step, ws, ms_e2e)
     return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
 
@@ -275,13 +308,12 @@ def run_gpu(args, w, window):
     import attention_sink_softmax_gb300 as sa
 
     ws, rank, local = dist_env()
-    if ws > 1:
-        torch.distributed.init_process_group("nccl")
+    init_dist(ws, "nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
 
-    prob_host = inputs.make_inputs(w, seed=w.seed + rank)
+    prob_host = inputs.make_inputs(w, seed=rank_seed(w, rank))
     d = {k: (v.to(dev) if v is not None else None) for k, v in prob_host.items()}
     q, k, v, sinks, dout, cu = d["q"], d["k"], d["v"], d["sinks"], d["dout"], d["cu_seqlens"]
     p = sa.make_params(q, k, cu, max_seqlen=w.seqlen, causal=w.causal, window=window,
@@ -339,7 +371,7 @@ def run_gpu(args, w, window):
 
     f_fwd, f_bwd = flops_of(w, window)
     flops_step = f_fwd + f_bwd
-    value = flops_step * ws / (ms / 1000) / 1e12
+    value = aggregate_value(flops_step, ws, ms)
 
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
@@ -365,11 +397,7 @@ def run_gpu(args, w, window):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen, "h_q": w.h_q,
-                   "h_kv": w.h_kv, "head_dim": w.head_dim, "causal": w.causal,
-                   "window": window, "tokens": w.total_tokens,
-                   "flops_per_step": flops_step, "l2": "inputs exceed L2 (no flush)",
-                   "parallelism": f"replicas x{ws} (independent batches, no collective)"},
+        "config": config_of(w, window, ws),
         "pct_of_peak": {"burst": 100 * value / ws / pk["bf16_tflops"],
                         "sustained": 100 * value / ws / pk["bf16_tflops_sustained"],
                         "source": pk_src},
@@ -384,8 +412,7 @@ def run_gpu(args, w, window):
         line["cpu_baseline"] = {"value": info["value"], "unit": "TFLOP/s", "cores": info["cores"],
                                 "kind": "oracle", "sample": info["sample"],
                                 "seconds": info["seconds"]}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    emit(line, rank)
     if ws > 1:
         torch.distributed.destroy_process_group()
 

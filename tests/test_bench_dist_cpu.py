@@ -1,0 +1,86 @@
+"""The benchmark's multi-rank path (one process per GPU, replicas with no
+data-path collective) run as two gloo ranks on the CPU: rank discovery, the
+per-rank batch seeds, the barrier, max-over-ranks timing, the whole-job
+aggregate and the rule that rank 0 alone prints."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+from attention_sink_softmax_gb300 import inputs
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, ws, port, outdir):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(ws), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    got_ws, got_rank, got_local = bench.dist_env()
+    bench.init_dist(got_ws, "gloo")
+    w = inputs.workload(0)
+    prob = inputs.make_inputs(w, seed=bench.rank_seed(w, got_rank))
+    bench.barrier(got_ws)
+    # each rank's step time; the job is as slow as its slowest rank
+    ms_local = 2.0 + 3.0 * got_rank
+    ms = bench.max_over_ranks(ms_local, got_ws, torch.device("cpu"))
+    flops = sum(bench.flops_of(w, w.window))
+    value = bench.aggregate_value(flops, got_ws, ms)
+    printed = bench.emit({"value": value, "rank": got_rank}, got_rank)
+    torch.save({"ws": got_ws, "rank": got_rank, "local": got_local, "ms": ms, "value": value,
+                "printed": printed, "q0": prob["q"].flatten()[:8].clone()},
+               os.path.join(outdir, f"r{rank}.pt"))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_gloo_ranks(tmp_path):
+    ws, port = 2, _free_port()
+    mp.spawn(_rank_main, args=(ws, port, str(tmp_path)), nprocs=ws, join=True)
+    r = [torch.load(os.path.join(tmp_path, f"r{i}.pt")) for i in range(ws)]
+    assert [x["rank"] for x in r] == [0, 1] and all(x["ws"] == 2 for x in r)
+    assert [x["local"] for x in r] == [0, 1]
+    # max over ranks: both see the slow rank's 5 ms
+    assert r[0]["ms"] == r[1]["ms"] == 5.0
+    w = inputs.workload(0)
+    flops = sum(bench.flops_of(w, w.window))
+    assert r[0]["value"] == pytest.approx(flops * 2 / 5e-3 / 1e12)
+    # rank 0 alone prints; the line is valid JSON
+    assert r[1]["printed"] is None
+    assert json.loads(r[0]["printed"])["rank"] == 0
+    # replicas draw different batches (weak scaling, no shared data)
+    assert not torch.equal(r[0]["q0"], r[1]["q0"])
+
+
+def test_reference_arm_rank_nonzero_does_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    def boom(*a, **k):  # the oracle must not run on rank 1
+        raise AssertionError("rank 1 ran the oracle")
+
+    monkeypatch.setattr(bench, "time_oracle", boom)
+    args = type("A", (), {"gpus": 2, "steps": 1, "warmup": 0})()
+    w = inputs.workload(0)
+    bench.run_reference(args, w, w.window)
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_matches_gpu_arm_config(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    args = type("A", (), {"gpus": 1, "steps": 1, "warmup": 0})()
+    w = inputs.workload(0)
+    bench.run_reference(args, w, w.window)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.config_of(w, w.window, 1)
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
