@@ -15,6 +15,7 @@ instead (the only reference this method has), on a bounded sample.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -71,8 +72,11 @@ def peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle-reason samples, every 100 ms, each with its
+    timestamp; ``summary`` keeps the samples taken inside [mark_start,
+    mark_end] (the timed region). nvidia-smi is started before the region and
+    given up to 3 s to produce its first sample."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -80,17 +84,27 @@ class ClockSampler:
         self.idx = device_index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 3.0
+            while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+                time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -113,6 +127,19 @@ class ClockSampler:
         os.unlink(self.file.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        if self.t0 is not None and self.t1 is not None:
+            kept = []
+            for r in rows:
+                try:
+                    ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if self.t0 <= ts <= self.t1:
+                    kept.append(r)
+            rows = kept
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no sample inside the timed region"],
+                    "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -355,11 +382,13 @@ def run_gpu(args, w, window):
     barrier(ws)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize(dev)
+        clk.mark_start()
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     barrier(ws)
     launches = sa.sink_attn_kernel_launches() - launches0
     ms_local = start.elapsed_time(end) / args.steps
@@ -420,7 +449,7 @@ def run_gpu(args, w, window):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=1, help="workload index 0..4")
