@@ -213,9 +213,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tc_fence_after();
             float p[64];  // P^T for this key and query rows [64w, 64w+64)
             {
-                uint32_t s0[32], s1[32];
-                tmem_ld32(tmem + lane_off + kColSdP + 64 * w, s0);
-                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32, s1);
+                uint32_t sv[64];
+                tmem_ld64(tmem + lane_off + kColSdP + 64 * w, sv);
                 tmem_ld_wait();
                 // S^T is in registers: dP^T may now be written into the same columns
                 tc_fence_before();
@@ -228,7 +227,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     const float4 l4 = *reinterpret_cast<const float4*>(&sm.lse[st][64 * w + j]);
                     const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nlog2e2);
                     const uint64_t nl23 = f2_mul(f2_pack(l4.z, l4.w), nlog2e2);
-                    const uint32_t* src = j < 32 ? s0 + j : s1 + (j - 32);
+                    const uint32_t* src = sv + j;
                     const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), sc2, nl01);
                     const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(src[2]), __uint_as_float(src[3])), sc2, nl23);
                     float x0, x1, x2, x3;
@@ -260,9 +259,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (!ok) break;
             tc_fence_after();
             {
-                uint32_t d0[32], d1[32];
-                tmem_ld32(tmem + lane_off + kColSdP + 64 * w, d0);
-                tmem_ld32(tmem + lane_off + kColSdP + 64 * w + 32, d1);
+                uint32_t dv64[64];
+                tmem_ld64(tmem + lane_off + kColSdP + 64 * w, dv64);
                 // P^T and dS^T are read by the previous step's dV and dK products, and
                 // this step's dS buffer by the dQ product of two steps back: poll their
                 // barriers now, while the loads are in flight, and wait below if needed
@@ -273,7 +271,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 for (int j = 0; j < 64; j += 4) {
                     // dS = P (dP - delta), two columns per paired op
                     const float4 D4 = *reinterpret_cast<const float4*>(&sm.delta[st][64 * w + j]);
-                    const uint32_t* d = j < 32 ? d0 + j : d1 + (j - 32);
+                    const uint32_t* d = dv64 + j;
                     const uint64_t t01 = f2_sub(f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1])),
                                                 f2_pack(D4.x, D4.y));
                     const uint64_t t23 = f2_sub(f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3])),
