@@ -34,10 +34,11 @@
 // of step i-1. A Q / dO stage is refilled once both issuers are done with it.
 //
 // Warps: 0-7 elementwise (thread = key = tensor-memory lane; warpgroup w takes
-// query rows [64w, 64w+64) of the step); 8 producer (TMA for K, Q, dO and
-// cp.async for the step's LSE and delta rows, through a kQStages ring); 9 and
-// 10 MMA issuers (one thread each); 12-15 dQ drain (tensor memory -> shared
-// staging -> TMA bulk reduce-add). Tensor memory: S^T/dP^T 0..127, dV
+// query rows [64w, 64w+64) of the step); 8 producer (TMA for K, Q, dO, and the
+// step's LSE and delta rows written as the B tiles of the extra K step, through
+// a kQStages ring); 9 and 10 MMA issuers (one thread each); 12-15 dQ drain
+// (tensor memory -> shared staging, 32 columns at a time -> TMA bulk
+// reduce-add). Tensor memory: S^T/dP^T 0..127, dV
 // 128..191, dK 192..255, dQ 256..319, K 320..351, V 352..383, P^T 384..447,
 // dS^T 448..511.
 #include <cudaTypedefs.h>
@@ -74,6 +75,29 @@ static_assert(2 * 128 * kEltRegs + 128 * kCtlRegs + 128 * kDqRegs <= kThreads * 
 constexpr uint32_t kColSdP = 0, kColDV = 128, kColDK = 192, kColDQ = 256, kColK = 320,
                    kColV = 352, kColP = 384, kColDS = 448;
 
+// LSE and delta reach the elementwise warps through the MMAs: one extra K = 16
+// step is appended to S^T = K Q^T and to dP^T = V dO^T, whose A operand holds
+// 1 in k = 0, 1, 2 of every key row and whose B operand holds, per query row,
+// -LSE / scale (resp. -delta) split into three bf16 parts (hi + mid + lo carry
+// about 24 bits). The accumulators then hold S - LSE / scale and dP - delta,
+// so P = exp2(S' * scale * log2 e) and dS = P dP' need no per-column loads.
+// The tiles are 128 rows x 16 bf16 without swizzle: element (r, k) at
+// aug_off(r) + (k / 8) * 128 + (k % 8) * 2.
+constexpr uint32_t kAugTile = 128 * 16 * 2;
+constexpr uint32_t kAugLBO = 128, kAugSBO = 256;
+__device__ __forceinline__ uint32_t aug_off(int r) { return (uint32_t)((r & 7) * 16 + (r >> 3) * 256); }
+
+// three bf16 parts whose sum is v to about 24 bits, packed (k = 0, 1, 2, 3 = 0)
+__device__ __forceinline__ uint2 split3_bf16(float v) {
+    const __nv_bfloat16 a = __float2bfloat16_rn(v);
+    float r = v - __bfloat162float(a);
+    const __nv_bfloat16 b = __float2bfloat16_rn(r);
+    r -= __bfloat162float(b);
+    const __nv_bfloat16 c = __float2bfloat16_rn(r);
+    return make_uint2((uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16),
+                      (uint32_t)__bfloat16_as_ushort(c));
+}
+
 struct BwdSmem {
     alignas(1024) __nv_bfloat16 k[kBN * kD];  // B operand of dQ
     alignas(1024) __nv_bfloat16 q[kQStages][kBM * kD];
@@ -81,10 +105,11 @@ struct BwdSmem {
     // dS, double-buffered by step parity: two 16 KB atoms (query rows 0..63 and
     // 64..127), each 128 keys x 128 bytes
     alignas(1024) uint8_t ds[2][2][kBN * 128];
-    // dQ block staged for the bulk reduce: columns 0..31 and 32..63, 128 rows x 128 bytes
-    alignas(1024) uint8_t dq_stage[2][kBM * 128];
-    alignas(16) float lse[kQStages][kBM];  // rows past the sequence hold a clamped copy
-    alignas(16) float delta[kQStages][kBM];
+    // half a dQ block (32 columns) staged for the bulk reduce, 128 rows x 128 bytes
+    alignas(1024) uint8_t dq_stage[kBM * 128];
+    alignas(128) uint8_t aug_ones[kAugTile];              // A of the extra K step
+    alignas(128) uint8_t aug_lse[kQStages][kAugTile];     // B: -LSE / scale, per query row
+    alignas(128) uint8_t aug_delta[kQStages][kAugTile];   // B: -delta, per query row
     uint64_t k_full, kv_tmem;
     uint64_t q_full[kQStages], q_empty[kQStages];
     uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, pd_free, ds_free[2], grads_done,
@@ -199,6 +224,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 row[4 * j + 3] = x.w;
             }
             tmem_st32(tmem + lane_off + (w == 0 ? kColK : kColV), row);
+            if (w == 0) {
+                // A of the extra K step: 1 in k = 0, 1, 2 of this key's row
+                uint8_t* ones = sm.aug_ones + aug_off(kr);
+                *reinterpret_cast<uint4*>(ones) = make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);
+                *reinterpret_cast<uint4*>(ones + 128) = make_uint4(0u, 0u, 0u, 0u);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.kv_tmem);
@@ -219,17 +251,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // S^T is in registers: dP^T may now be written into the same columns
                 tc_fence_before();
                 mbar_arrive(&sm.s_loaded);
-                // P = exp2(S * scale * log2 e - LSE * log2 e), two columns per paired op
+                // P = exp2((S - LSE / scale) * scale * log2 e), two columns per paired op
                 const uint64_t sc2 = f2_pack(sc, sc);
-                const uint64_t nlog2e2 = f2_pack(-kLog2e, -kLog2e);
 #pragma unroll
                 for (int j = 0; j < 64; j += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(&sm.lse[st][64 * w + j]);
-                    const uint64_t nl01 = f2_mul(f2_pack(l4.x, l4.y), nlog2e2);
-                    const uint64_t nl23 = f2_mul(f2_pack(l4.z, l4.w), nlog2e2);
                     const uint32_t* src = sv + j;
-                    const uint64_t a01 = f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), sc2, nl01);
-                    const uint64_t a23 = f2_fma(f2_pack(__uint_as_float(src[2]), __uint_as_float(src[3])), sc2, nl23);
+                    const uint64_t a01 = f2_mul(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), sc2);
+                    const uint64_t a23 = f2_mul(f2_pack(__uint_as_float(src[2]), __uint_as_float(src[3])), sc2);
                     float x0, x1, x2, x3;
                     f2_unpack(a01, x0, x1);
                     f2_unpack(a23, x2, x3);
@@ -269,13 +297,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 64; j += 4) {
-                    // dS = P (dP - delta), two columns per paired op
-                    const float4 D4 = *reinterpret_cast<const float4*>(&sm.delta[st][64 * w + j]);
+                    // dS = P (dP - delta), two columns per paired op (the MMA subtracted delta)
                     const uint32_t* d = dv64 + j;
-                    const uint64_t t01 = f2_sub(f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1])),
-                                                f2_pack(D4.x, D4.y));
-                    const uint64_t t23 = f2_sub(f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3])),
-                                                f2_pack(D4.z, D4.w));
+                    const uint64_t t01 = f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1]));
+                    const uint64_t t23 = f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3]));
                     float y0, y1, y2, y3;
                     f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t01), y0, y1);
                     f2_unpack(f2_mul(f2_pack(p[j + 2], p[j + 3]), t23), y2, y3);
@@ -348,31 +373,31 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // one decision for all four drain warps (they meet at named barriers below)
             if (!vote_all_128(1, wait_phase(&sm.grads_done, it & 1, flags, abort_word))) break;
             tc_fence_after();
-            // the previous step's reduce must have read the staging buffer
-            if (issuer) bulk_wait_read<0>();
-            named_barrier_sync(1, 128);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                // the previous reduce must have read the staging buffer
+                if (issuer) bulk_wait_read<0>();
+                named_barrier_sync(1, 128);
                 uint32_t a[32];
                 tmem_ld32(tmem + lane_off + kColDQ + 32 * half, a);
                 tmem_ld_wait();
                 if (half == 1) {
+                    // the dQ columns have been read: the next dQ product may overwrite them
                     tc_fence_before();
                     mbar_arrive(&sm.dq_consumed);
                 }
 #pragma unroll
                 for (int c16 = 0; c16 < 8; ++c16)
-                    *reinterpret_cast<uint4*>(sm.dq_stage[half] + sw128(r, c16 * 16)) =
+                    *reinterpret_cast<uint4*>(sm.dq_stage + sw128(r, c16 * 16)) =
                         make_uint4(a[4 * c16], a[4 * c16 + 1], a[4 * c16 + 2], a[4 * c16 + 3]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            named_barrier_sync(1, 128);
-            if (issuer) {
-                // rows past the sequence carry exact zeros (their dS is 0), so adding
-                // them into the next sequence's rows changes nothing
-                tma_reduce_add_3d(&tmDQ, sm.dq_stage[0], 0, h, start + q0);
-                tma_reduce_add_3d(&tmDQ, sm.dq_stage[1], 32, h, start + q0);
-                bulk_commit();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                named_barrier_sync(1, 128);
+                if (issuer) {
+                    // rows past the sequence carry exact zeros (their dS is 0), so adding
+                    // them into the next sequence's rows changes nothing
+                    tma_reduce_add_3d(&tmDQ, sm.dq_stage, 32 * half, h, start + q0);
+                    bulk_commit();
+                }
             }
         }
         if (issuer) bulk_wait_all<0>();
@@ -387,6 +412,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
                 tma_load_3d(sm.k, &tmK, &sm.k_full, 0, hk, start + k0);
             }
+            // B tiles of the extra K step: only k = 0..3 of each row are rewritten per step
+            for (int i = lane; i < (int)(kQStages * kAugTile / 16); i += 32) {
+                reinterpret_cast<uint4*>(sm.aug_lse)[i] = make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(sm.aug_delta)[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();  // every lane's zeros land before any lane writes a row
+            const float neg_inv_scale = -1.f / P.scale;
             int issued = 0;
             for (int it = 0; it < nsteps; ++it) {
                 const int st = it % kQStages;
@@ -401,18 +433,25 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     tma_load_3d(sm.q[st], &tmQ, &sm.q_full[st], 0, h, start + q0);
                     tma_load_3d(sm.dout[st], &tmDO, &sm.q_full[st], 0, h, start + q0);
                 }
+                float lv[kBM / 32], dv_[kBM / 32];
 #pragma unroll
                 for (int u = 0; u < kBM / 32; ++u) {
                     const int c = lane * (kBM / 32) + u;
                     const int ip = min(q0 + c, L - 1);  // rows past the sequence are masked
                     const size_t ix = (size_t)h * P.total + start + ip;
-                    cp_async4(&sm.lse[st][c], lse + ix);
-                    cp_async4(&sm.delta[st][c], delta + ix);
+                    lv[u] = __ldg(lse + ix);
+                    dv_[u] = __ldg(delta + ix);
                 }
-                cp_async_arrive(&sm.q_full[st]);
+#pragma unroll
+                for (int u = 0; u < kBM / 32; ++u) {
+                    const int c = lane * (kBM / 32) + u;
+                    *reinterpret_cast<uint2*>(sm.aug_lse[st] + aug_off(c)) = split3_bf16(lv[u] * neg_inv_scale);
+                    *reinterpret_cast<uint2*>(sm.aug_delta[st] + aug_off(c)) = split3_bf16(-dv_[u]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&sm.q_full[st]);
                 issued = it + 1;
             }
-            asm volatile("cp.async.wait_all;" ::: "memory");
             if (lane == 0) {
                 drain_phase(&sm.k_full, 0);
                 for (int it = max(0, issued - kQStages); it < issued; ++it)
@@ -421,14 +460,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         } else if (warp == 9 && lane == 0) {
             // -------------------------------------------------------- MMA issuer 1: S^T, dP^T
             constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // A tmem, B K-major
+            const uint64_t dones = smem_desc_noswizzle(smem_u32(sm.aug_ones), kAugLBO, kAugSBO);
             bool ok = wait_phase(&sm.kv_tmem, 0, flags, abort_word) &&
                       wait_phase(&sm.q_full[0], 0, flags, abort_word);
-            auto issue_s = [&](int st) {  // S^T = K Q^T
+            auto issue_s = [&](int st) {  // S^T - LSE / scale = K Q^T + ones (-LSE / scale)^T
                 tc_fence_after();
                 const uint64_t dq_ = smem_desc_sw128(smem_u32(sm.q[st]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     mma_ts(tmem + kColSdP, tmem + kColK + kk * 8, dq_ + 2 * kk, idSS, kk > 0);
+                mma_ss(tmem + kColSdP, dones, smem_desc_noswizzle(smem_u32(sm.aug_lse[st]), kAugLBO, kAugSBO),
+                       idSS, 1);
                 mma_commit(&sm.s_full);
             };
             if (ok) issue_s(0);
@@ -438,12 +480,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // early poll of the next step's Q / dO stage (answer used after dP)
                 const bool q_ready = it + 1 >= nsteps || mbar_test_wait(&sm.q_full[st1], ((it + 1) / kQStages) & 1);
                 if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
-                // dP^T = V dO^T into the columns S^T was read from
+                // dP^T - delta = V dO^T + ones (-delta)^T, into the columns S^T was read from
                 tc_fence_after();
                 const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     mma_ts(tmem + kColSdP, tmem + kColV + kk * 8, ddo + 2 * kk, idSS, kk > 0);
+                mma_ss(tmem + kColSdP, dones, smem_desc_noswizzle(smem_u32(sm.aug_delta[st]), kAugLBO, kAugSBO),
+                       idSS, 1);
                 mma_commit(&sm.dp_full);
                 mma_commit(&sm.q_empty[st]);  // this issuer's last read of the step's Q / dO stage
                 if (it + 1 < nsteps) {

@@ -260,6 +260,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Shared-memory descriptor without swizzle (K-major): the operand is made of
+// 8-row x 16-byte core matrices, each stored as 128 contiguous bytes; LBO is
+// the byte distance between core matrices adjacent along K, SBO between core
+// matrices adjacent along M/N. Element (row r, k) of a 16-wide tile with
+// LBO = 128 and SBO = 256 sits at (r%8)*16 + (r/8)*256 + (k/8)*128 + (k%8)*2.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo_bytes,
+                                                        uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate:
 //   [4,6) D format 1 = f32; [7,10) A format 1 = bf16; [10,13) B format 1 = bf16;
 //   [15] A major (0 = K-major, 1 = MN-major); [16] B major;
