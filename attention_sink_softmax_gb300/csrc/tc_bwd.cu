@@ -322,16 +322,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (!ok) break;
                 }
             }
-            tc_fence_after();
-            tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
-            tmem_st32(tmem + lane_off + kColDS + 32 * w, pd);
-            // dS row of this key: 64 query rows = 128 bytes of atom w (A operand of dQ)
+            // dS row of this key: 64 query rows = 128 bytes of atom w (A operand of dQ);
+            // written before the tensor-memory stores so that the proxy fence below
+            // finds them done
             uint8_t* atom = sm.ds[it & 1][w];
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) {
                 const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
                 *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
             }
+            tc_fence_after();
+            tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
+            tmem_st32(tmem + lane_off + kColDS + 32 * w, pd);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             // poll the next step's S^T while the stores drain
             s_ready = it + 1 < nsteps && mbar_test_wait(&sm.s_full, (it + 1) & 1);
