@@ -238,7 +238,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bool ok = true;
         bool s_ready = false;  // S^T of this step seen complete by an early poll
         for (int it = 0; it < nsteps; ++it) {
-            const int st = it % kQStages;
             const int q0 = (qb_lo + it % nq) * kBM;
             ok = __all_sync(0xffffffffu, s_ready || wait_phase(&sm.s_full, it & 1, flags, abort_word));
             if (!ok) break;
