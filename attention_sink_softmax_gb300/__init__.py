@@ -29,7 +29,8 @@ __all__ = [
     "sink_attn_fwd", "sink_attn_bwd", "sink_attn_bwd_preprocess", "sink_attn_bwd_main",
     "sink_attn_fetch_device_error", "sink_attn_bwd_preprocess_noalloc",
     "sink_attn_noalloc_scratch_bytes", "sink_attn_status_str", "sink_attn_kernel_launches",
-    "sink_attn_version",
+    "sink_attn_version", "make_decode_params", "sink_attn_decode_workspace_bytes",
+    "sink_attn_decode",
     "sink_attention", "SinkAttentionFunction",
 ]
 
@@ -227,6 +228,64 @@ def sink_attn_bwd_preprocess_noalloc(params, sinks, o, lse, dout, *, delta=None,
 
 def sink_attn_noalloc_scratch_bytes() -> int:
     return int(lib().sink_attn_noalloc_scratch_bytes())
+
+
+def make_decode_params(q: torch.Tensor, k_cache: torch.Tensor, max_seqlen: int, window: int = 0,
+                       softmax_scale: Optional[float] = None) -> SinkAttnParams:
+    """sink_attn_params_t for sink_attn_decode: q [B, H_q, d], k_cache [T, H_kv, d];
+    ``max_seqlen`` bounds every context length."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if q.dim() != 3 or k_cache.dim() != 3:
+        raise ValueError("q must be [B, H_q, d] and the cache [T, H_kv, d]")
+    p = SinkAttnParams()
+    p.batch, p.h_q, p.head_dim = q.shape
+    p.total_tokens, p.h_kv = k_cache.shape[0], k_cache.shape[1]
+    p.max_seqlen = int(max_seqlen)
+    p.dtype = _DTYPES[q.dtype]
+    p.softmax_scale = float(softmax_scale) if softmax_scale is not None else 0.0
+    p.causal = 1
+    p.window = int(window) if window else 0
+    return p
+
+
+def sink_attn_decode_workspace_bytes(params: SinkAttnParams) -> int:
+    return int(lib().sink_attn_decode_workspace_bytes(ctypes.byref(params)))
+
+
+def sink_attn_decode(q, k_cache, v_cache, sinks, kv_start, kv_len, *, max_seqlen=None, window=0,
+                     softmax_scale=None, out=None, lse=None, workspace=None, stream=None,
+                     params=None):
+    """Decode: one query per entry against a key/value cache; returns (o, lse).
+    See sink_attn_decode in include/sink_attn.h. ``max_seqlen`` None reads the
+    largest of ``kv_len`` (synchronises)."""
+    _need_cuda("q", q)
+    _need_cuda("k_cache", k_cache, q.dtype)
+    _need_cuda("v_cache", v_cache, q.dtype)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    _need_cuda("sinks", sinks, torch.float32)
+    _need_cuda("kv_start", kv_start, torch.int32)
+    _need_cuda("kv_len", kv_len, torch.int32)
+    if max_seqlen is None:
+        max_seqlen = int(kv_len.max()) if kv_len.numel() else 0
+    p = params or make_decode_params(q, k_cache, max_seqlen, window, softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((p.h_q, p.batch), dtype=torch.float32, device=q.device)
+    need = sink_attn_decode_workspace_bytes(p)
+    if need == 0:
+        raise SinkAttnError(_abi.SINK_ERR_INVALID_ARG, "sink_attn_decode_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    st = lib().sink_attn_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sinks),
+                                _ptr(kv_start), _ptr(kv_len), _ptr(out), _ptr(lse), _ptr(workspace),
+                                workspace.numel(), _stream(stream, q.device))
+    _abi.check(st, "sink_attn_decode")
+    return out, lse
 
 
 def sink_attn_fetch_device_error(workspace: torch.Tensor, stream=None):

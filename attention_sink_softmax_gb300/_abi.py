@@ -34,6 +34,8 @@ EXPORTS = (
     "sink_attn_fetch_device_error",
     "sink_attn_bwd_preprocess_noalloc",
     "sink_attn_noalloc_scratch_bytes",
+    "sink_attn_decode_workspace_bytes",
+    "sink_attn_decode",
     "sink_attn_status_str",
     "sink_attn_kernel_launches",
     "sink_attn_version",
@@ -104,6 +106,10 @@ def lib():
             L.sink_attn_bwd_preprocess_noalloc.restype = ctypes.c_int
             L.sink_attn_noalloc_scratch_bytes.argtypes = []
             L.sink_attn_noalloc_scratch_bytes.restype = ctypes.c_size_t
+            L.sink_attn_decode_workspace_bytes.argtypes = [_PP]
+            L.sink_attn_decode_workspace_bytes.restype = ctypes.c_size_t
+            L.sink_attn_decode.argtypes = [_PP] + [_P] * 8 + [_P, ctypes.c_size_t, _P]
+            L.sink_attn_decode.restype = ctypes.c_int
             L.sink_attn_status_str.argtypes = [ctypes.c_int]
             L.sink_attn_status_str.restype = ctypes.c_char_p
             L.sink_attn_kernel_launches.argtypes = []

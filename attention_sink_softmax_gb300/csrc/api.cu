@@ -230,6 +230,64 @@ sink_status_t sink_attn_fetch_device_error(void* workspace, size_t workspace_byt
     return SINK_OK;
 }
 
+namespace {
+// Decode: [header][partials], the split count fixed by the params so that the
+// workspace size needs no device query.
+DecodeArgs decode_args(const sink_attn_params_t* p) {
+    DecodeArgs a;
+    a.batch = p->batch;
+    a.h_q = p->h_q;
+    a.h_kv = p->h_kv;
+    a.group = p->h_q / p->h_kv;
+    a.total = p->total_tokens;
+    a.max_len = p->max_seqlen;
+    a.window = p->window > 0 ? p->window : 0;
+    a.nsplit = decode_splits(p->batch, p->h_kv, p->max_seqlen);
+    const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)p->head_dim);
+    a.scale_log2 = scale * kLog2e;
+    return a;
+}
+
+size_t decode_bytes(const sink_attn_params_t* p) {
+    return kHeaderBytes + align_up(sizeof(float) * decode_partial_floats(p->batch, p->h_q));
+}
+
+sink_status_t validate_decode(const sink_attn_params_t* p) {
+    sink_status_t st = validate(p);
+    if (st != SINK_OK) return st;
+    if (!p->causal) return SINK_ERR_INVALID_ARG;  // the query is the last token of its context
+    if (p->h_q / p->h_kv > 64) return SINK_ERR_UNSUPPORTED;  // query heads per key/value head
+    return SINK_OK;
+}
+}  // namespace
+
+size_t sink_attn_decode_workspace_bytes(const sink_attn_params_t* params) {
+    if (validate_decode(params) != SINK_OK) return 0;
+    return decode_bytes(params);
+}
+
+sink_status_t sink_attn_decode(const sink_attn_params_t* params, const void* q, const void* k_cache,
+                               const void* v_cache, const float* sinks, const int32_t* kv_start,
+                               const int32_t* kv_len, void* o, float* lse, void* workspace,
+                               size_t workspace_bytes, sink_stream_t stream) {
+    sink_status_t st = validate_decode(params);
+    if (st != SINK_OK) return st;
+    if (!workspace || !aligned16(workspace) || !device_accessible(workspace)) return SINK_ERR_WORKSPACE;
+    if (workspace_bytes < decode_bytes(params)) return SINK_ERR_WORKSPACE;
+    if (params->batch == 0) return SINK_OK;
+    if (!all_aligned({q, o, (const void*)sinks, (const void*)lse})) return SINK_ERR_INVALID_ARG;
+    if (params->total_tokens > 0 && !all_aligned({k_cache, v_cache})) return SINK_ERR_INVALID_ARG;
+    for (const int32_t* x : {kv_start, kv_len})
+        if (!x || ((uintptr_t)x & 3u) || !device_accessible(x)) return SINK_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t* flags = (uint32_t*)workspace;
+    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return SINK_ERR_CUDA;
+    e = decode(decode_args(params), params->dtype == SINK_BF16, q, k_cache, v_cache, sinks, kv_start,
+               kv_len, o, lse, (float*)((char*)workspace + kHeaderBytes), flags, s);
+    return cuda_status(e);
+}
+
 const char* sink_attn_status_str(sink_status_t status) {
     switch (status) {
         case SINK_OK: return "ok";

@@ -31,6 +31,18 @@ struct Problem {
     const int32_t* cu; // device cu_seqlens or nullptr (padded: sequence s = [s*N, s*N+N))
 };
 
+// Decode (one query per entry against a key/value cache), see decode.cu.
+constexpr int kDecodeMaxSplits = 64;
+struct DecodeArgs {
+    int batch;        // queries
+    int h_q, h_kv, group;
+    int total;        // rows of the cache
+    int max_len;      // upper bound on every kv_len
+    int window;       // <= 0: whole context; W: its last W keys
+    int nsplit;       // chunks of each query's keys
+    float scale_log2;
+};
+
 __device__ __forceinline__ void seq_bounds(const Problem& P, int s, int& start, int& len) {
     if (P.cu) {
         start = __ldg(P.cu + s);

@@ -146,3 +146,45 @@ def random_problem(seed: int, lengths, h_q: int, h_kv: int, head_dim: int,
         cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
     return dict(q=q, k=k, v=v, sinks=sinks, dout=dout, cu_seqlens=cu)
+
+
+@dataclass
+class DecodeWorkload:
+    """Decode: `batch` newest tokens, each against its own `ctx`-token context in
+    a shared key/value cache (contexts back to back)."""
+    name: str
+    batch: int
+    ctx: int
+    h_q: int
+    h_kv: int
+    head_dim: int
+    dtype: torch.dtype
+    window: int
+    seed: int
+    scale: float = 0.125
+
+    @property
+    def cache_tokens(self) -> int:
+        return self.batch * self.ctx
+
+
+def decode_workload() -> DecodeWorkload:
+    """Streaming inference on the GPT-OSS-20B layer shape: 8 sequences whose
+    contexts are 32768 tokens (the long-context workload's length)."""
+    return DecodeWorkload("decode_B8_ctx32768_Hq64_Hkv8_d64_bf16", 8, 32768, 64, 8, 64,
+                          torch.bfloat16, 0, 7)
+
+
+def make_decode_inputs(w: DecodeWorkload, *, device: str = "cpu") -> dict:
+    """q [batch, h_q, d], k/v cache [batch * ctx, h_kv, d] ~ N(0,1) in w.dtype,
+    sinks [h_q] ~ N(0,1) fp32, kv_start / kv_len int32 [batch]."""
+    g = torch.Generator().manual_seed(w.seed)
+    T = w.cache_tokens
+    q = torch.randn(w.batch, w.h_q, w.head_dim, generator=g).to(w.dtype)
+    k = torch.randn(T, w.h_kv, w.head_dim, generator=g).to(w.dtype)
+    v = torch.randn(T, w.h_kv, w.head_dim, generator=g).to(w.dtype)
+    sinks = torch.randn(w.h_q, generator=g).float()
+    kv_start = torch.arange(w.batch, dtype=torch.int32) * w.ctx
+    kv_len = torch.full((w.batch,), w.ctx, dtype=torch.int32)
+    out = dict(q=q, k=k, v=v, sinks=sinks, kv_start=kv_start, kv_len=kv_len)
+    return {n: t.to(device) for n, t in out.items()}

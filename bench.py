@@ -446,6 +446,67 @@ def run_gpu(args, w, window):
         torch.distributed.destroy_process_group()
 
 
+def run_decode(args):
+    """Decode (one newest token per sequence against its KV cache): bandwidth of
+    sink_attn_decode on the decode workload, device-timed, one JSON line. Not
+    the headline metric; the roofline is HBM (the cache is read once)."""
+    import attention_sink_softmax_gb300 as sa
+
+    ws_, rank, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    w = inputs.decode_workload()
+    d = inputs.make_decode_inputs(w, device=str(dev))
+    p = sa.make_decode_params(d["q"], d["k"], max_seqlen=w.ctx, window=w.window, softmax_scale=w.scale)
+    work = torch.empty(sa.sink_attn_decode_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(w.h_q, w.batch, dtype=torch.float32, device=dev)
+
+    def step():
+        sa.sink_attn_decode(d["q"], d["k"], d["v"], d["sinks"], d["kv_start"], d["kv_len"], params=p,
+                            out=o, lse=lse, workspace=work, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    steps = 10 * args.steps  # a decode step is short: keep the timed region long enough to sample clocks
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark_end()
+    st, flags = sa.sink_attn_fetch_device_error(work)
+    if st != 0:
+        raise RuntimeError(f"device flagged an error: status {st}, flags {flags}")
+    ms = start.elapsed_time(end) / steps
+    esz = d["q"].element_size()
+    cache = 2 * w.cache_tokens * w.h_kv * w.head_dim * esz  # K and V, each read once
+    qo = 2 * w.batch * w.h_q * w.head_dim * esz + 4 * w.h_q * w.batch
+    gbs = (cache + qo) / (ms / 1000) / 1e9
+    pk, pk_src = peaks()
+    line = {
+        "metric": "sink-attention decode bandwidth (bf16 KV cache read once)", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "context": w.ctx, "h_q": w.h_q, "h_kv": w.h_kv,
+                   "head_dim": w.head_dim, "window": w.window, "bytes_per_step": cache + qo,
+                   "l2": "KV cache exceeds L2 (no flush)"},
+        "clocks": clk.summary(),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "decode_split_kernel",
+                     "peak_kind": f"HBM copy ({pk_src})"},
+    }
+    emit(line, rank)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,10 +517,14 @@ def main():
     ap.add_argument("--window", type=int, default=None, help="override the workload's window")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--decode", action="store_true",
+                    help="measure the decode path (KV-cache bandwidth) instead of the training step")
     args = ap.parse_args()
     w = inputs.workload(args.config)
     window = w.window if args.window is None else args.window
-    if args.impl == "reference":
+    if args.decode:
+        run_decode(args)
+    elif args.impl == "reference":
         run_reference(args, w, window)
     else:
         run_gpu(args, w, window)

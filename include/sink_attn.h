@@ -172,6 +172,38 @@ SINK_API sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t
 /* Size in bytes of the fixed scratch array used by the _noalloc entry point. */
 SINK_API size_t sink_attn_noalloc_scratch_bytes(void);
 
+/* Decode / streaming inference: one query per entry b against a key/value
+ * cache. The page's sinks exist for streaming inference (section
+ * "FlashAttentionV3对注意力槽的支持"), and its section "纠正训练与推理不一致问题"
+ * (Fig. 4) measures the gap between the training and inference attention
+ * paths; this is the inference path, and its o and lse for query b equal row
+ * kv_len[b] - 1 of sink_attn_fwd on the same context (same definitions as
+ * above: the sink joins the denominator once, adds no value row, and lse
+ * includes it).
+ * Query b is the last token of its context, cache rows kv_start[b] ..
+ * kv_start[b] + kv_len[b] - 1; it sees all of them, or the last `window` of
+ * them when window > 0.
+ * Params: batch = number of queries; total_tokens = rows of the cache;
+ * max_seqlen = an upper bound on every kv_len; h_q, h_kv, head_dim (64),
+ * dtype, softmax_scale, window; causal must be 1.
+ * Layouts (device memory): q, o [batch, h_q, d]; k_cache, v_cache
+ * [total_tokens, h_kv, d]; sinks [h_q] fp32; lse [h_q, batch] fp32;
+ * kv_start, kv_len int32 [batch] (4-byte aligned); the others 16-byte aligned.
+ * The keys of each query are split into chunks whose partial results
+ * (without the sink) are merged with the sink counted once; the workspace
+ * (sink_attn_decode_workspace_bytes) holds the partials; it needs no
+ * initialisation. A query whose kv_len is < 1 or > max_seqlen, or whose
+ * context runs past the end of the cache, reads no key: it gets the result
+ * of an empty key set (o = 0, lse = S_h), and the flag word reports
+ * SINK_ERR_DEVICE through sink_attn_fetch_device_error. */
+SINK_API size_t sink_attn_decode_workspace_bytes(const sink_attn_params_t* params);
+SINK_API sink_status_t sink_attn_decode(const sink_attn_params_t* params,
+                                        const void* q, const void* k_cache, const void* v_cache,
+                                        const float* sinks, const int32_t* kv_start,
+                                        const int32_t* kv_len, void* o, float* lse,
+                                        void* workspace, size_t workspace_bytes,
+                                        sink_stream_t stream);
+
 /* Static description of a status code. Never NULL. */
 SINK_API const char* sink_attn_status_str(sink_status_t status);
 

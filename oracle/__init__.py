@@ -185,3 +185,33 @@ def row(q, k, v, sinks, *, seq, head, i, dout=None, scale=None, causal=True, win
     if n < 0:
         raise ValueError("sink_oracle_row: invalid argument")
     return first.value, p[: n + 1].copy(), (dz[: n + 1].copy() if dout is not None else None)
+
+
+def decode(q, k_cache, v_cache, sinks, kv_start, kv_len, *, scale=None, window=0):
+    """Decode oracle: query b (q [B, H_q, d]) is the last token of the context
+    k_cache / v_cache [kv_start[b] : kv_start[b] + kv_len[b]] ([T, H_kv, d]);
+    returns (o [B, H_q, d], lse [H_q, B]) in fp64.
+
+    No arithmetic of its own: for each query it evaluates row kv_len[b] - 1 of
+    the forward above on that context (the query placed in that row), which is
+    what a streaming decoder computes for the newest token.
+    """
+    q, k_cache, v_cache, sinks = _f64(q), _f64(k_cache), _f64(v_cache), _f64(sinks)
+    B, h_q, d = q.shape
+    h_kv = k_cache.shape[1]
+    o = np.zeros((B, h_q, d), dtype=np.float64)
+    lse = np.zeros((h_q, B), dtype=np.float64)
+    starts = np.asarray(kv_start, dtype=np.int64).reshape(-1)
+    lens = np.asarray(kv_len, dtype=np.int64).reshape(-1)
+    for b in range(B):
+        s0, n = int(starts[b]), int(lens[b])
+        if n < 1 or s0 < 0 or s0 + n > k_cache.shape[0]:
+            raise ValueError("decode: context outside the cache")
+        qq = np.zeros((n, h_q, d), dtype=np.float64)
+        qq[n - 1] = q[b]
+        ob, lb = forward(qq, k_cache[s0:s0 + n], v_cache[s0:s0 + n], sinks, scale=scale, causal=True,
+                         window=window, cu_seqlens=np.array([0, n], dtype=np.int32),
+                         row_begin=n - 1, row_end=n)
+        o[b] = ob[n - 1]
+        lse[:, b] = lb[:, n - 1]
+    return o, lse

@@ -109,3 +109,16 @@ def test_python_layer_rejects_cpu_tensors(L):
     k = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         sa.sink_attn_fwd(q, k, k, torch.zeros(2))
+
+
+def test_decode_workspace_and_validation(L):
+    p = _params(batch=8, max_seqlen=32768, total_tokens=262144)
+    need = sa.sink_attn_decode_workspace_bytes(p)
+    # header + 64 chunks x 8 queries x 64 heads x (m, l, o[64]) fp32
+    assert need >= 256 + 4 * 64 * 8 * 64 * 66 and need % 256 == 0
+    assert sa.sink_attn_decode_workspace_bytes(_params(causal=0)) == 0
+    assert sa.sink_attn_decode_workspace_bytes(_params(head_dim=128)) == 0
+    nul = ctypes.c_void_p(0)
+    assert L.sink_attn_decode(ctypes.byref(_params(causal=0)), *([nul] * 8), nul, 0, nul) == \
+        _abi.SINK_ERR_INVALID_ARG
+    assert L.sink_attn_decode(ctypes.byref(p), *([nul] * 8), nul, 0, nul) == _abi.SINK_ERR_WORKSPACE

@@ -364,3 +364,68 @@ def test_rejects_invalid_arguments():
         oracle.forward(q, k, k, np.zeros(2), cu_seqlens=np.array([0, 3, 2, 4], dtype=np.int32))
     with pytest.raises(ValueError):
         oracle.forward(np.zeros((4, 3, 8)), k[:, :1].repeat(2, 1), k[:, :1].repeat(2, 1), np.zeros(3))
+
+
+# ----------------------------------------------------------------------------- decode
+def _decode_problem(rng, lengths, h_q, h_kv, d, sink_scale=1.0):
+    """A shared cache holding every context back to back, one query per context."""
+    T = int(sum(lengths)) + 3
+    k = rng.standard_normal((T, h_kv, d))
+    v = rng.standard_normal((T, h_kv, d))
+    q = rng.standard_normal((len(lengths), h_q, d))
+    sinks = sink_scale * rng.standard_normal(h_q)
+    starts = np.concatenate([[2], 2 + np.cumsum(lengths)[:-1]]).astype(np.int64)
+    return q, k, v, sinks, starts, np.asarray(lengths, dtype=np.int64)
+
+
+@pytest.mark.parametrize("window", [0, 5])
+def test_decode_with_sink_at_minus_infinity_is_sdpa_of_one_query(window):
+    """S_h -> -inf: the newest token attends like plain softmax attention
+    (torch's scaled_dot_product_attention) over its context or window."""
+    rng = np.random.default_rng(31)
+    q, k, v, _, starts, lens = _decode_problem(rng, [1, 9, 40], 4, 2, 16)
+    sinks = np.full(4, -1e30)
+    o, lse = oracle.decode(q, k, v, sinks, starts, lens, scale=0.25, window=window)
+    for b, (s0, n) in enumerate(zip(starts, lens)):
+        lo = max(0, n - window) if window else 0
+        kk = torch.tensor(k[s0 + lo:s0 + n]).repeat_interleave(2, dim=1).permute(1, 0, 2)
+        vv = torch.tensor(v[s0 + lo:s0 + n]).repeat_interleave(2, dim=1).permute(1, 0, 2)
+        qq = torch.tensor(q[b])[:, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=0.25)[:, 0]
+        np.testing.assert_allclose(o[b], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_decode_window_one_is_a_sigmoid_of_the_newest_key():
+    """Window 1: one key j against the sink: O = sigmoid(s - S_h) v_j, and
+    LSE = log(exp(s) + exp(S_h))."""
+    rng = np.random.default_rng(32)
+    q, k, v, sinks, starts, lens = _decode_problem(rng, [5, 12], 2, 1, 8)
+    o, lse = oracle.decode(q, k, v, sinks, starts, lens, scale=0.5, window=1)
+    for b, (s0, n) in enumerate(zip(starts, lens)):
+        j = s0 + n - 1
+        for h in range(2):
+            s = 0.5 * float(q[b, h] @ k[j, 0])
+            sig = 1.0 / (1.0 + math.exp(-(s - sinks[h])))
+            np.testing.assert_allclose(o[b, h], sig * v[j, 0], rtol=1e-12, atol=1e-14)
+            assert lse[h, b] == pytest.approx(math.log(math.exp(s) + math.exp(sinks[h])), rel=1e-13)
+
+
+def test_decode_equals_the_row_routine_on_every_prefix():
+    """Streaming one sequence token by token gives each row of the training
+    forward: checked against the oracle's separate single-row routine
+    (combined probabilities over the row's keys and the sink)."""
+    rng = np.random.default_rng(33)
+    L, h_q, h_kv, d = 24, 4, 2, 8
+    q, k, v, sinks, dout = _rand_problem(rng, L, h_q, h_kv, d)
+    cu = np.array([0, L], dtype=np.int32)
+    for window in (0, 6):
+        o, lse = oracle.decode(q, k, v, sinks, np.zeros(L, np.int64), np.arange(1, L + 1),
+                               scale=0.3, window=window)
+        for i in range(L):
+            for h in range(h_q):
+                first, p, _ = oracle.row(q, k, v, sinks, seq=0, head=h, i=i, scale=0.3, causal=True,
+                                         window=window, cu_seqlens=cu)
+                keys = np.arange(first, first + len(p) - 1)
+                np.testing.assert_allclose(o[i, h], p[:-1] @ v[keys, h // 2], rtol=1e-12, atol=1e-14)
+                # LSE from the sink's probability: P_sink = exp(S_h - LSE)
+                assert lse[h, i] == pytest.approx(sinks[h] - math.log(p[-1]), rel=1e-12, abs=1e-12)
