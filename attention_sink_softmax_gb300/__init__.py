@@ -267,9 +267,11 @@ def sink_attn_decode(q, k_cache, v_cache, sinks, kv_start, kv_len, *, max_seqlen
     _need_cuda("sinks", sinks, torch.float32)
     _need_cuda("kv_start", kv_start, torch.int32)
     _need_cuda("kv_len", kv_len, torch.int32)
-    if max_seqlen is None:
-        max_seqlen = int(kv_len.max()) if kv_len.numel() else 0
-    p = params or make_decode_params(q, k_cache, max_seqlen, window, softmax_scale)
+    if params is None:
+        if max_seqlen is None:  # synchronises: pass max_seqlen or params inside a graph capture
+            max_seqlen = int(kv_len.max()) if kv_len.numel() else 0
+        params = make_decode_params(q, k_cache, max_seqlen, window, softmax_scale)
+    p = params
     if out is None:
         out = torch.empty_like(q)
     if lse is None:

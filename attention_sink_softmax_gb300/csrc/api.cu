@@ -248,8 +248,14 @@ DecodeArgs decode_args(const sink_attn_params_t* p) {
     return a;
 }
 
+// [header][per (query, key/value head) chunk counters][partials]; the header
+// and the counters are zeroed together by one memset per call.
+size_t decode_counter_bytes(const sink_attn_params_t* p) {
+    return align_up(sizeof(int32_t) * (size_t)p->batch * p->h_kv);
+}
 size_t decode_bytes(const sink_attn_params_t* p) {
-    return kHeaderBytes + align_up(sizeof(float) * decode_partial_floats(p->batch, p->h_q));
+    return kHeaderBytes + decode_counter_bytes(p) +
+           align_up(sizeof(float) * decode_partial_floats(p->batch, p->h_q));
 }
 
 sink_status_t validate_decode(const sink_attn_params_t* p) {
@@ -281,10 +287,12 @@ sink_status_t sink_attn_decode(const sink_attn_params_t* params, const void* q, 
         if (!x || ((uintptr_t)x & 3u) || !device_accessible(x)) return SINK_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t* flags = (uint32_t*)workspace;
-    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t), s);
+    const size_t counters = decode_counter_bytes(params);
+    cudaError_t e = cudaMemsetAsync(flags, 0, kHeaderBytes + counters, s);
     if (e != cudaSuccess) return SINK_ERR_CUDA;
     e = decode(decode_args(params), params->dtype == SINK_BF16, q, k_cache, v_cache, sinks, kv_start,
-               kv_len, o, lse, (float*)((char*)workspace + kHeaderBytes), flags, s);
+               kv_len, o, lse, (float*)((char*)workspace + kHeaderBytes + counters),
+               (int32_t*)((char*)workspace + kHeaderBytes), flags, s);
     return cuda_status(e);
 }
 

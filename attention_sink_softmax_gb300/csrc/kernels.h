@@ -25,12 +25,13 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
                            const float* lse, const void* dout, float* delta, float* dsinks,
                            float* partial, cudaStream_t st);
 
-// Decode: split kernel + merge kernel (decode.cu). `part` holds
-// decode_partial_floats(batch, h_q) floats.
+// Decode (decode.cu): split kernel (+ merge kernel on the CUDA-core path).
+// `part` holds decode_partial_floats(batch, h_q) floats; `counters` holds
+// batch x h_kv int32 that are zero on entry and zero again on exit.
 int decode_splits(int batch, int h_kv, int max_len);
 size_t decode_partial_floats(int batch, int h_q);
 cudaError_t decode(const DecodeArgs& a, bool bf16, const void* q, const void* k, const void* v,
                    const float* sinks, const int32_t* kv_start, const int32_t* kv_len, void* o,
-                   float* lse, float* part, uint32_t* flags, cudaStream_t st);
+                   float* lse, float* part, int32_t* counters, uint32_t* flags, cudaStream_t st);
 
 }  // namespace sinkattn

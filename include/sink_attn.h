@@ -191,8 +191,12 @@ SINK_API size_t sink_attn_noalloc_scratch_bytes(void);
  * kv_start, kv_len int32 [batch] (4-byte aligned); the others 16-byte aligned.
  * The keys of each query are split into chunks whose partial results
  * (without the sink) are merged with the sink counted once; the workspace
- * (sink_attn_decode_workspace_bytes) holds the partials; it needs no
- * initialisation. A query whose kv_len is < 1 or > max_seqlen, or whose
+ * (sink_attn_decode_workspace_bytes) holds the partials and one chunk counter
+ * per (query, key/value head). It needs no initialisation: the call zeroes
+ * the flag word and the counters on the stream first, so calls that share a
+ * workspace must be ordered on one stream. The call only enqueues stream work
+ * (one memset, one or two kernels), so it may be captured in a CUDA graph.
+ * A query whose kv_len is < 1 or > max_seqlen, or whose
  * context runs past the end of the cache, reads no key: it gets the result
  * of an empty key set (o = 0, lse = S_h), and the flag word reports
  * SINK_ERR_DEVICE through sink_attn_fetch_device_error. */

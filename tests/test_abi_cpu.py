@@ -114,8 +114,9 @@ def test_python_layer_rejects_cpu_tensors(L):
 def test_decode_workspace_and_validation(L):
     p = _params(batch=8, max_seqlen=32768, total_tokens=262144)
     need = sa.sink_attn_decode_workspace_bytes(p)
-    # header + 64 chunks x 8 queries x 64 heads x (m, l, o[64]) fp32
-    assert need >= 256 + 4 * 64 * 8 * 64 * 66 and need % 256 == 0
+    # header + a chunk counter per (query, key/value head) + 64 chunks x 8
+    # queries x 64 heads x (m, l, o[64]) fp32
+    assert need >= 256 + 4 * 8 * 8 + 4 * 64 * 8 * 64 * 66 and need % 256 == 0
     assert sa.sink_attn_decode_workspace_bytes(_params(causal=0)) == 0
     assert sa.sink_attn_decode_workspace_bytes(_params(head_dim=128)) == 0
     nul = ctypes.c_void_p(0)

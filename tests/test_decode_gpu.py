@@ -49,6 +49,7 @@ CASES = [
     ([2048, 33], 8, 1),       # MQA-like group of 8
     ([513, 64], 16, 1),       # group of 16: two query heads per warp
     ([100, 257], 4, 4),       # MHA
+    ([300, 77], 32, 1),       # group of 32: the CUDA-core kernel for bf16 too
 ]
 
 
@@ -62,6 +63,29 @@ def test_decode_parity(dtype, window, lengths, h_q, h_kv):
                                    window=window)
     assert_close("decode O", o, o_ref, dtype)
     assert_close("decode LSE", lse, lse_ref, dtype, rounds_output=False)
+
+
+@pytest.mark.parametrize("window", [0, 100])
+def test_decode_reads_nothing_outside_the_context(window):
+    """Every cache row outside the contexts holds NaN, and the last context
+    ends at the cache's last row (its final 32-key box runs past the cache):
+    the result must match the oracle computed on the clean cache."""
+    q, k, v, sinks, starts, lens = _problem(11, [45, 1000, 33], 8, 2, torch.bfloat16, gap=1)
+    lens[-1] = k.shape[0] - int(starts[-1])  # the last context runs to the end of the cache
+    o_ref, lse_ref = oracle.decode(q, k, v, sinks, starts.numpy(), lens.numpy(), scale=0.125,
+                                   window=window)
+    inside = torch.zeros(k.shape[0], dtype=torch.bool)
+    for st, n in zip(starts.tolist(), lens.tolist()):
+        inside[st:st + n] = True
+    assert not inside.all()
+    k_bad, v_bad = k.clone(), v.clone()
+    k_bad[~inside] = float("nan")
+    v_bad[~inside] = float("nan")
+    o, lse = _run(q, k_bad, v_bad, sinks, starts, lens, window)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    assert_close("decode O (NaN outside the contexts)", o, o_ref, torch.bfloat16)
+    assert_close("decode LSE (NaN outside the contexts)", lse, lse_ref, torch.bfloat16,
+                 rounds_output=False)
 
 
 def test_decode_full_size_sampled_queries():
@@ -141,3 +165,26 @@ def test_decode_rejects_host_pointers():
     d = [t.to(DEV) for t in (q, k, v, sinks)]
     with pytest.raises(ValueError):
         sa.sink_attn_decode(*d, starts, lens.to(DEV))  # kv_start left on the host
+
+
+def test_decode_under_cuda_graph_capture_matches_eager():
+    """The C-ABI call only enqueues work on the caller's stream, so a run of
+    decode calls captured into a CUDA graph and replayed gives the eager
+    result bit for bit."""
+    q, k, v, sinks, starts, lens = _problem(13, [700, 64, 2000], 16, 2, torch.bfloat16)
+    d = [t.to(DEV) for t in (q, k, v, sinks, starts, lens)]
+    p = sa.make_decode_params(d[0], d[1], max_seqlen=2000)
+    ws = torch.empty(sa.sink_attn_decode_workspace_bytes(p), dtype=torch.uint8, device=DEV)
+    o_e, lse_e = sa.sink_attn_decode(*d, params=p, workspace=ws)
+    torch.cuda.synchronize()
+    o_g, lse_g = torch.empty_like(o_e), torch.empty_like(lse_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        sa.sink_attn_decode(*d, params=p, out=o_g, lse=lse_g, workspace=ws,
+                            stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, o_e) and torch.equal(lse_g, lse_e)
+    assert sa.sink_attn_fetch_device_error(ws)[0] == _abi.SINK_OK
