@@ -213,6 +213,20 @@ def source_digest(paths):
     return h.hexdigest()[:16]
 
 
+# The sources each profiled kernel is built from (its traffic entry is valid
+# while their digest is the one the counters were taken on).
+KERNEL_SOURCES = {
+    "bwd_main": ["common.cuh", "tc.h", "tc_bwd.cu", "tc_common.cuh", "tc_ptx.cuh"],
+    "fwd": ["common.cuh", "tc.h", "tc_fwd.cu", "tc_common.cuh", "tc_ptx.cuh"],
+    "decode": ["common.cuh", "decode.cu", "tc_common.cuh", "tc_ptx.cuh"],
+}
+
+
+def kernel_sources(stage):
+    csrc = os.path.join(ROOT, "attention_sink_softmax_gb300", "csrc")
+    return [os.path.join(csrc, f) for f in KERNEL_SOURCES[stage]]
+
+
 def profiled_traffic(kernel_source, stage):
     """DRAM traffic per launch from the committed ncu summary, if the kernel's
     source is unchanged since it was captured; else None."""
@@ -412,10 +426,7 @@ def run_gpu(args, w, window):
     # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop
     main_ms = stage_ms[2]
     main_tflops = f_bwd / (main_ms / 1000) / 1e12
-    csrc = os.path.join(ROOT, "attention_sink_softmax_gb300", "csrc")
-    main_src = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
-                      if f.endswith((".cu", ".cuh", ".h")))
-    traffic = profiled_traffic(main_src, "bwd_main")
+    traffic = profiled_traffic(kernel_sources("bwd_main"), "bwd_main")
     roofline = {"bound": "tensor", "achieved": main_tflops,
                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
@@ -526,7 +537,8 @@ def run_decode(args):
                    "l2": "KV cache exceeds L2 (no flush)", "launch": launch},
         "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "decode_mma_kernel",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(kernel_sources("decode"), "decode"),
+                     "kernel": "decode_mma_kernel",
                      "peak_kind": f"HBM copy ({pk_src})"},
     }
     emit(line, rank)
