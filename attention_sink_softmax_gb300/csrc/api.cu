@@ -57,7 +57,7 @@ sink_status_t validate(const sink_attn_params_t* p) {
     // sizes must keep every element index and every grid dimension in range
     if ((int64_t)p->total_tokens * p->h_q * p->head_dim > ((int64_t)1 << 40)) return SINK_ERR_INVALID_ARG;
     if (p->batch > 65535 || p->h_q > 65535) return SINK_ERR_UNSUPPORTED;
-    if (p->head_dim != 64) return SINK_ERR_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128) return SINK_ERR_UNSUPPORTED;
     return SINK_OK;
 }
 
@@ -263,6 +263,7 @@ sink_status_t validate_decode(const sink_attn_params_t* p) {
     if (st != SINK_OK) return st;
     if (!p->causal) return SINK_ERR_INVALID_ARG;  // the query is the last token of its context
     if (p->h_q / p->h_kv > 64) return SINK_ERR_UNSUPPORTED;  // query heads per key/value head
+    if (p->head_dim != 64) return SINK_ERR_UNSUPPORTED;      // the decode kernels are 64-wide
     return SINK_OK;
 }
 }  // namespace

@@ -80,7 +80,7 @@ sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t* p, cons
     if (!p || p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv || p->total_tokens < 0)
         return SINK_ERR_INVALID_ARG;
     if (p->dtype != SINK_BF16 && p->dtype != SINK_FP32) return SINK_ERR_INVALID_ARG;
-    if (p->head_dim != 64) return SINK_ERR_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128) return SINK_ERR_UNSUPPORTED;
     const size_t need = (size_t)p->h_q * (size_t)preprocess_chunks(p->total_tokens);
     if (need > kNoallocScratchFloats) return SINK_ERR_SCRATCH_LIMIT;
     if (!ok_ptr(sinks) || !ok_ptr(dsinks)) return SINK_ERR_INVALID_ARG;

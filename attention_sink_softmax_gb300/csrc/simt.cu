@@ -16,11 +16,13 @@
 
 namespace sinkattn {
 
-constexpr int kD = 64;          // head_dim handled by these kernels
+// Every kernel is instantiated for head_dim kD = 64 and 128 (a thread keeps
+// rows of kD fp32 values in registers; at 128 some of them live in local
+// memory).
 constexpr int kFwdRows = 128;   // query rows per block (one thread each)
 constexpr int kFwdKeys = 32;    // keys per shared-memory tile
 
-template <typename T>
+template <typename T, int kD>
 __global__ void __launch_bounds__(kFwdRows)
 simt_fwd_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
                 const T* __restrict__ v, const float* __restrict__ sinks,
@@ -106,9 +108,9 @@ simt_fwd_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
 // ---------------------------------------------------------------------------
 // Backward step 1: delta = rowsum(dO * O) in [h_q, T] and per-chunk partials of
 // sum_t exp(S_h - LSE_t) * delta_t. One block = one head x kPreTokens tokens;
-// 8 lanes share one 64-wide row, each lane one 16-byte (bf16) or 32-byte
-// (fp32) piece. All of a thread's loads are issued before any is used, so
-// every thread keeps kPreIters rows of O and dO in flight (memory-bound step).
+// kD / 8 lanes share one row, each lane one 16-byte (bf16) or 32-byte (fp32)
+// piece of 8 elements. A thread issues the loads of 8 of its rows before using
+// any, so every thread keeps 8 rows of O and dO in flight (memory-bound step).
 constexpr int kPreTokens = 256;
 constexpr int kPreThreads = 256;
 
@@ -151,46 +153,50 @@ __device__ __forceinline__ float dot_piece(const Piece8<float>& a, const Piece8<
     return s;
 }
 
-template <typename T>
+template <typename T, int kD>
 __global__ void __launch_bounds__(kPreThreads)
 preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restrict__ dout,
                   const float* __restrict__ lse, const float* __restrict__ sinks,
                   float* __restrict__ delta, float* __restrict__ partial) {
-    constexpr int kLanes = 8;  // threads per row
-    constexpr int kPer = kD / kLanes;
+    constexpr int kLanes = kD / 8;  // threads per row, 8 elements each
+    constexpr int kPer = 8;
     constexpr int kRowsPerIter = kPreThreads / kLanes;
     constexpr int kIters = kPreTokens / kRowsPerIter;
+    constexpr int kBatch = 8;  // rows of a thread in flight at once
+    static_assert(kIters % kBatch == 0, "row batches");
     __shared__ float warp_sum[kPreThreads / 32];
     const int h = blockIdx.y;
     const int t0 = blockIdx.x * kPreTokens;
     const int sub = threadIdx.x % kLanes;
     const int r0 = threadIdx.x / kLanes;
     const float sink = __ldg(sinks + h);
-    Piece8<T> po[kIters], pd[kIters];
-    float lz[kIters];
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-        const int t = t0 + r0 + it * kRowsPerIter;
-        if (t < total) {
-            const size_t off = ((size_t)t * h_q + h) * kD + sub * kPer;
-            po[it] = load_piece(o + off);
-            pd[it] = load_piece(dout + off);
-            lz[it] = __ldg(lse + (size_t)h * total + t);
-        }
-    }
     float mine = 0.f;  // this row-group's running sum, added in token order
+    for (int b0 = 0; b0 < kIters; b0 += kBatch) {
+        Piece8<T> po[kBatch], pd[kBatch];
+        float lz[kBatch];
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-        const int t = t0 + r0 + it * kRowsPerIter;
-        float dsum = t < total ? dot_piece(po[it], pd[it]) : 0.f;
+        for (int x = 0; x < kBatch; ++x) {
+            const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
+            if (t < total) {
+                const size_t off = ((size_t)t * h_q + h) * kD + sub * kPer;
+                po[x] = load_piece(o + off);
+                pd[x] = load_piece(dout + off);
+                lz[x] = __ldg(lse + (size_t)h * total + t);
+            }
+        }
 #pragma unroll
-        for (int w = kLanes / 2; w >= 1; w >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, w);
-        if (t < total) {
-            if (sub == 0) delta[(size_t)h * total + t] = dsum;
-            mine += expf(sink - lz[it]) * dsum;
+        for (int x = 0; x < kBatch; ++x) {
+            const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
+            float dsum = t < total ? dot_piece(po[x], pd[x]) : 0.f;
+#pragma unroll
+            for (int w = kLanes / 2; w >= 1; w >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, w);
+            if (t < total) {
+                if (sub == 0) delta[(size_t)h * total + t] = dsum;
+                mine += expf(sink - lz[x]) * dsum;
+            }
         }
     }
-    // fixed-order reduction: lanes 0, 8, 16, 24 of each warp, then warps in order
+    // fixed-order reduction: the first lane of each row group, then warps in order
     if (sub != 0) mine = 0.f;
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, w);
@@ -218,7 +224,7 @@ __global__ void dsink_reduce_kernel(int h_q, int nchunks, const float* __restric
 constexpr int kDqRows = 128;
 constexpr int kDqKeys = 32;
 
-template <typename T>
+template <typename T, int kD>
 __global__ void __launch_bounds__(kDqRows)
 simt_dq_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
                const T* __restrict__ v, const float* __restrict__ lse,
@@ -283,15 +289,19 @@ simt_dq_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
     }
 }
 
-constexpr int kKvKeys = 64;   // keys per block (one thread each)
-constexpr int kKvRows = 16;   // query rows per shared-memory tile
+// keys per block (one thread each) and query rows per shared-memory tile,
+// sized so that the static shared memory stays under 48 KB
+template <int kD> constexpr int kv_keys() { return kD == 64 ? 64 : 32; }
+template <int kD> constexpr int kv_rows() { return kD == 64 ? 16 : 8; }
 
-template <typename T>
-__global__ void __launch_bounds__(kKvKeys)
+template <typename T, int kD>
+__global__ void __launch_bounds__(kv_keys<kD>())
 simt_dkdv_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
                  const T* __restrict__ v, const float* __restrict__ lse,
                  const float* __restrict__ delta, const T* __restrict__ dout,
                  T* __restrict__ dk, T* __restrict__ dv) {
+    constexpr int kKvKeys = kv_keys<kD>();
+    constexpr int kKvRows = kv_rows<kD>();
     __shared__ float kown[kKvKeys][kD + 1];
     __shared__ float vown[kKvKeys][kD + 1];
     __shared__ float qs[kKvRows][kD];
@@ -368,13 +378,13 @@ simt_dkdv_kernel(Problem P, const T* __restrict__ q, const T* __restrict__ k,
 // ---------------------------------------------------------------------------
 // Host launchers.
 
-template <typename T>
+template <typename T, int kD>
 static cudaError_t launch_fwd_t(const Problem& P, const void* q, const void* k, const void* v,
                                 const float* sinks, void* o, float* lse, uint32_t* flags,
                                 cudaStream_t st) {
     dim3 grid((P.max_seqlen + kFwdRows - 1) / kFwdRows, P.h_q, P.nseq);
-    simt_fwd_kernel<T><<<grid, kFwdRows, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v, sinks,
-                                                  (T*)o, lse, flags);
+    simt_fwd_kernel<T, kD><<<grid, kFwdRows, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
+                                                      sinks, (T*)o, lse, flags);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -382,8 +392,11 @@ static cudaError_t launch_fwd_t(const Problem& P, const void* q, const void* k, 
 cudaError_t simt_fwd(const Problem& P, bool bf16, const void* q, const void* k, const void* v,
                      const float* sinks, void* o, float* lse, uint32_t* flags, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
-    return bf16 ? launch_fwd_t<__nv_bfloat16>(P, q, k, v, sinks, o, lse, flags, st)
-                : launch_fwd_t<float>(P, q, k, v, sinks, o, lse, flags, st);
+    if (P.head_dim == 128)
+        return bf16 ? launch_fwd_t<__nv_bfloat16, 128>(P, q, k, v, sinks, o, lse, flags, st)
+                    : launch_fwd_t<float, 128>(P, q, k, v, sinks, o, lse, flags, st);
+    return bf16 ? launch_fwd_t<__nv_bfloat16, 64>(P, q, k, v, sinks, o, lse, flags, st)
+                : launch_fwd_t<float, 64>(P, q, k, v, sinks, o, lse, flags, st);
 }
 
 int preprocess_chunks(int total) { return (total + kPreTokens - 1) / kPreTokens; }
@@ -394,12 +407,20 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
     const int nchunks = preprocess_chunks(P.total);
     if (nchunks > 0) {
         dim3 grid(nchunks, P.h_q);
-        if (bf16)
-            preprocess_kernel<__nv_bfloat16><<<grid, kPreThreads, 0, st>>>(
+        const bool d128 = P.head_dim == 128;
+        if (bf16 && d128)
+            preprocess_kernel<__nv_bfloat16, 128><<<grid, kPreThreads, 0, st>>>(
                 P.total, P.h_q, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse, sinks,
                 delta, partial);
+        else if (bf16)
+            preprocess_kernel<__nv_bfloat16, 64><<<grid, kPreThreads, 0, st>>>(
+                P.total, P.h_q, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse, sinks,
+                delta, partial);
+        else if (d128)
+            preprocess_kernel<float, 128><<<grid, kPreThreads, 0, st>>>(
+                P.total, P.h_q, (const float*)o, (const float*)dout, lse, sinks, delta, partial);
         else
-            preprocess_kernel<float><<<grid, kPreThreads, 0, st>>>(
+            preprocess_kernel<float, 64><<<grid, kPreThreads, 0, st>>>(
                 P.total, P.h_q, (const float*)o, (const float*)dout, lse, sinks, delta, partial);
         count_launches(1);
         cudaError_t e = cudaGetLastError();
@@ -410,19 +431,20 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, int kD>
 static cudaError_t launch_bwd_t(const Problem& P, const void* q, const void* k, const void* v,
                                 const float* lse, const float* delta, const void* dout, void* dq,
                                 void* dk, void* dv, cudaStream_t st) {
     dim3 gq((P.max_seqlen + kDqRows - 1) / kDqRows, P.h_q, P.nseq);
-    simt_dq_kernel<T><<<gq, kDqRows, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v, lse, delta,
-                                              (const T*)dout, (T*)dq);
+    simt_dq_kernel<T, kD><<<gq, kDqRows, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v, lse,
+                                                  delta, (const T*)dout, (T*)dq);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 gk((P.max_seqlen + kKvKeys - 1) / kKvKeys, P.h_kv, P.nseq);
-    simt_dkdv_kernel<T><<<gk, kKvKeys, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v, lse,
-                                                delta, (const T*)dout, (T*)dk, (T*)dv);
+    constexpr int kKeys = kv_keys<kD>();
+    dim3 gk((P.max_seqlen + kKeys - 1) / kKeys, P.h_kv, P.nseq);
+    simt_dkdv_kernel<T, kD><<<gk, kKeys, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v, lse,
+                                                  delta, (const T*)dout, (T*)dk, (T*)dv);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -431,8 +453,11 @@ cudaError_t simt_bwd_main(const Problem& P, bool bf16, const void* q, const void
                           const float* lse, const float* delta, const void* dout, void* dq,
                           void* dk, void* dv, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
-    return bf16 ? launch_bwd_t<__nv_bfloat16>(P, q, k, v, lse, delta, dout, dq, dk, dv, st)
-                : launch_bwd_t<float>(P, q, k, v, lse, delta, dout, dq, dk, dv, st);
+    if (P.head_dim == 128)
+        return bf16 ? launch_bwd_t<__nv_bfloat16, 128>(P, q, k, v, lse, delta, dout, dq, dk, dv, st)
+                    : launch_bwd_t<float, 128>(P, q, k, v, lse, delta, dout, dq, dk, dv, st);
+    return bf16 ? launch_bwd_t<__nv_bfloat16, 64>(P, q, k, v, lse, delta, dout, dq, dk, dv, st)
+                : launch_bwd_t<float, 64>(P, q, k, v, lse, delta, dout, dq, dk, dv, st);
 }
 
 }  // namespace sinkattn

@@ -49,10 +49,12 @@ __device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
 
 }  // namespace tc
 
-// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token) with 128-byte
-// swizzle; box = box_rows tokens x 1 head x 64. Returns false if the driver's
-// encoder is unavailable or rejects the tensor.
-bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows);
+// [T, H, dim] bf16 viewed as a 3-D tensor (d, head, token) with 128-byte
+// swizzle; box = box_rows tokens x 1 head x 64 columns (dim = 64 or 128; a
+// 128-wide row is fetched as two boxes). Returns false if the driver's encoder
+// is unavailable or rejects the tensor.
+bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows,
+                        int dim = 64);
 
 // [T, H, 64] fp32 viewed the same way, box = box_rows tokens x 1 head x 32
 // floats (128 bytes, 128-byte swizzle): used to reduce-add dQ blocks.

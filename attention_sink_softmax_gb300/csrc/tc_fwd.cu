@@ -30,6 +30,11 @@
 // Tensor memory (512 columns): S_t at t*128, O_t at 256 + t*64, P_t (bf16
 // pairs) at 384 + t*64. Every mbarrier wait is bounded; a wait that gives up
 // sets the timeout flag and the CTA winds down without further work.
+//
+// Head dim D = 64 or 128. A tile of D columns is held as D/64 swizzle atoms
+// of 128 rows x 64 (128-byte rows), each filled by its own TMA box; S takes
+// D/16 K steps across the atoms, and P V is issued per atom (N = 64 each).
+// At D = 128 a CTA holds one tile (NT = 1): S 128 + O 128 + P 64 columns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -47,9 +52,11 @@ using namespace tc;
 
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per block
-constexpr int kD = 64;             // head dim
+constexpr int kAtomCols = 64;      // head-dim columns per 128-byte swizzle atom
+constexpr uint32_t kAtomBytes = kBM * kAtomCols * 2;  // 16 KB (kBM == kBN)
 constexpr int kStages = 3;         // K/V ring depth
-constexpr uint32_t kTileBytes = kBM * kD * 2;
+template <int D>
+constexpr uint32_t tile_bytes() { return kBM * D * 2; }
 constexpr float kRescaleLog2 = 8.0f;
 // Register split for two tiles (384 threads launched at kLaunchRegs each):
 // 2 softmax warpgroups x 128 x kSoftmaxRegs + 1 warpgroup x 128 x kOtherRegs
@@ -62,11 +69,11 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 384 * kLaunchRegs, "r
 template <int NT>
 constexpr int fwd_threads() { return NT * 128 + 128; }
 
-template <int NT>
+template <int NT, int D>
 struct FwdSmem {
-    alignas(1024) __nv_bfloat16 q[NT][kBM * kD];
-    alignas(1024) __nv_bfloat16 k[kStages][kBN * kD];
-    alignas(1024) __nv_bfloat16 v[kStages][kBN * kD];
+    alignas(1024) __nv_bfloat16 q[NT][kBM * D];  // D/64 atoms of 128 rows x 64
+    alignas(1024) __nv_bfloat16 k[kStages][kBN * D];
+    alignas(1024) __nv_bfloat16 v[kStages][kBN * D];
     uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
@@ -76,14 +83,21 @@ struct FwdSmem {
     int abort_flag;
 };
 
-template <int NT>
+static_assert(sizeof(FwdSmem<1, 128>) + 1024 <= 232448, "shared memory of the D = 128 forward");
+static_assert(sizeof(FwdSmem<2, 64>) + 1024 <= 232448, "shared memory of the D = 64 forward");
+
+template <int NT, int D>
 __global__ void __launch_bounds__(fwd_threads<NT>(), 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
               float* __restrict__ lse, uint32_t* flags) {
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(D == 64 || NT == 1, "tensor memory holds one D = 128 tile");
+    constexpr int kAtoms = D / kAtomCols;
+    constexpr uint32_t kTileBytes = tile_bytes<D>();
     extern __shared__ uint8_t smem_raw[];
-    FwdSmem<NT>& sm = *reinterpret_cast<FwdSmem<NT>*>(
+    FwdSmem<NT, D>& sm = *reinterpret_cast<FwdSmem<NT, D>*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int rb = gridDim.x - 1 - blockIdx.x;  // longest tiles first
@@ -229,17 +243,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             f2_unpack(rs2[3], r6, r7);
             const float rs = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
             if (i > 0 && __any_sync(0xffffffffu, upd)) {
-                uint32_t oa[32], ob[32];
-                tmem_ld32(tO, oa);
-                tmem_ld32(tO + 32, ob);
-                tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    oa[j] = __float_as_uint(__uint_as_float(oa[j]) * corr);
-                    ob[j] = __float_as_uint(__uint_as_float(ob[j]) * corr);
+                for (int c0 = 0; c0 < D; c0 += 64) {
+                    uint32_t oa[32], ob[32];
+                    tmem_ld32(tO + c0, oa);
+                    tmem_ld32(tO + c0 + 32, ob);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        oa[j] = __float_as_uint(__uint_as_float(oa[j]) * corr);
+                        ob[j] = __float_as_uint(__uint_as_float(ob[j]) * corr);
+                    }
+                    tmem_st32(tO + c0, oa);
+                    tmem_st32(tO + c0 + 32, ob);
                 }
-                tmem_st32(tO, oa);
-                tmem_st32(tO + 32, ob);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -252,31 +269,36 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             wait_phase(&sm.o_done[t], (nblk - 1) & 1, flags, abort_word));
         if (ok) {
             tc_fence_after();
-            uint32_t oa[32], ob[32];
-            tmem_ld32(tO, oa);
-            tmem_ld32(tO + 32, ob);
-            tmem_ld_wait();
+            const float inv = 1.f / l;
+            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t oa[32], ob[32];
+                tmem_ld32(tO + c0, oa);
+                tmem_ld32(tO + c0 + 32, ob);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(oa[8 * j + 0]) * inv, __uint_as_float(oa[8 * j + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(oa[8 * j + 2]) * inv, __uint_as_float(oa[8 * j + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(oa[8 * j + 4]) * inv, __uint_as_float(oa[8 * j + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(oa[8 * j + 6]) * inv, __uint_as_float(oa[8 * j + 7]) * inv);
+                        dst[c0 / 8 + j] = w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ob[8 * j + 0]) * inv, __uint_as_float(ob[8 * j + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(ob[8 * j + 2]) * inv, __uint_as_float(ob[8 * j + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(ob[8 * j + 4]) * inv, __uint_as_float(ob[8 * j + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(ob[8 * j + 6]) * inv, __uint_as_float(ob[8 * j + 7]) * inv);
+                        dst[c0 / 8 + 4 + j] = w;
+                    }
+                }
+            }
             if (valid) {
-                const float inv = 1.f / l;
-                uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * kD);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(oa[8 * j + 0]) * inv, __uint_as_float(oa[8 * j + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(oa[8 * j + 2]) * inv, __uint_as_float(oa[8 * j + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(oa[8 * j + 4]) * inv, __uint_as_float(oa[8 * j + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(oa[8 * j + 6]) * inv, __uint_as_float(oa[8 * j + 7]) * inv);
-                    dst[j] = w;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ob[8 * j + 0]) * inv, __uint_as_float(ob[8 * j + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(ob[8 * j + 2]) * inv, __uint_as_float(ob[8 * j + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(ob[8 * j + 4]) * inv, __uint_as_float(ob[8 * j + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(ob[8 * j + 6]) * inv, __uint_as_float(ob[8 * j + 7]) * inv);
-                    dst[4 + j] = w;
-                }
                 lse[(size_t)h * P.total + start + row] = (m + __log2f(l)) * kLn2;
             }
         }
@@ -289,7 +311,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
                 mbar_arrive_expect_tx(&sm.q_full, NT * kTileBytes);
-                for (int t = 0; t < NT; ++t) tma_load_3d(sm.q[t], &tmQ, &sm.q_full, 0, h0 + t, start + r0);
+                for (int t = 0; t < NT; ++t)
+                    for (int a = 0; a < kAtoms; ++a)
+                        tma_load_3d(sm.q[t] + a * kBM * kAtomCols, &tmQ, &sm.q_full, a * kAtomCols,
+                                    h0 + t, start + r0);
                 int issued = 0;
                 for (int i = 0; i < nblk; ++i) {
                     const int st = i % kStages;
@@ -298,9 +323,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         break;
                     const int kpos = start + (kb_lo + i) * kBN;
                     mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-                    tma_load_3d(sm.k[st], &tmK, &sm.k_full[st], 0, hk, kpos);
+                    for (int a = 0; a < kAtoms; ++a)
+                        tma_load_3d(sm.k[st] + a * kBN * kAtomCols, &tmK, &sm.k_full[st], a * kAtomCols,
+                                    hk, kpos);
                     mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                    tma_load_3d(sm.v[st], &tmV, &sm.v_full[st], 0, hk, kpos);
+                    for (int a = 0; a < kAtoms; ++a)
+                        tma_load_3d(sm.v[st] + a * kBN * kAtomCols, &tmV, &sm.v_full[st], a * kAtomCols,
+                                    hk, kpos);
                     issued = i + 1;
                 }
                 // copies still in flight must land before the CTA's shared memory goes away
@@ -314,16 +343,25 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         } else if (warp >= 4 * NT + 1 && warp <= 4 * NT + NT && lane == 0) {
             // ------------------------------------------------------------ MMA issuer of tile t
             const int t = warp - (4 * NT + 1);
-            constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);  // Q, K both K-major
-            constexpr uint32_t idO = idesc_bf16(kBM, kD, 0, 1);   // P from TMEM, V MN-major
-            const uint64_t dq = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
+            constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);       // Q, K both K-major
+            constexpr uint32_t idO = idesc_bf16(kBM, kAtomCols, 0, 1);  // P from TMEM, V MN-major
             const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
+            // K step kk of S reads atom kk / 4 at byte offset 32 (kk % 4); both are
+            // added to the descriptors' start-address field (16-byte units)
+            const uint64_t dq = smem_desc_sw128(smem_u32(sm.q[t]), 16, 1024);
+            auto s_product = [&](int stage) {
+                const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[stage]), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk / 4) * kAtomBytes) >> 4) + 2 * (kk % 4);
+                    mma_ss(tS, dq + off, dk + off, idS, kk > 0);
+                }
+            };
             bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
                       wait_phase(&sm.k_full[0], 0, flags, abort_word);
             if (ok) {
                 tc_fence_after();
-                const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
-                for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                s_product(0);
                 mma_commit(&sm.s_full[t]);
             }
             for (int i = 0; ok && i < nblk; ++i) {
@@ -335,8 +373,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word)))
                         break;
                     tc_fence_after();
-                    const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st1]), 16, 1024);
-                    for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tS, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+                    s_product(st1);
                     mma_commit(&sm.s_full[t]);
                 }
                 // O_t += P_t(i) V(i)
@@ -344,8 +381,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
                 tc_fence_after();
                 const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
+#pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tO, tP + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
+#pragma unroll
+                    for (int a = 0; a < kAtoms; ++a)
+                        mma_ts(tO + a * kAtomCols, tP + kk * 8,
+                               dv + (uint64_t)((a * kAtomBytes + kk * 16 * 128) >> 4), idO,
+                               (i > 0 || kk > 0));
                 mma_commit(&sm.o_done[t]);
                 // this tile's last reads of stage st (K(i) by S_t(i), V(i) by the product above)
                 mma_commit(&sm.kv_empty[st]);
@@ -380,13 +422,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [T, H, 64] bf16 viewed as a 3-D tensor (d, head, token); box = 128 tokens x 1 head.
-bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows) {
+// [T, H, dim] bf16 viewed as a 3-D tensor (d, head, token); box = 64 columns
+// (one 128-byte swizzle row) x 1 head x box_rows tokens.
+bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int heads, int box_rows,
+                        int dim) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)box_rows};
+    cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kAtomCols, 1, (cuuint32_t)box_rows};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -398,8 +442,8 @@ bool make_head_tile_map(CUtensorMap* map, const void* base, int tokens, int head
 bool make_f32_head_half_map(CUtensorMap* map, void* base, int tokens, int heads, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)heads * kD * 4};
+    cuuint64_t dims[3] = {64, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {64 * 4, (cuuint64_t)heads * 64 * 4};
     cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
@@ -408,29 +452,29 @@ bool make_f32_head_half_map(CUtensorMap* map, void* base, int tokens, int heads,
 }
 
 bool tc_fwd_supported(const Problem& P, bool bf16) {
-    return bf16 && P.head_dim == kD && encode_fn() != nullptr && P.total > 0;
+    return bf16 && (P.head_dim == 64 || P.head_dim == 128) && encode_fn() != nullptr && P.total > 0;
 }
 
 size_t tc_fwd_workspace_bytes(const Problem&, bool) { return 0; }
 
-template <int NT>
+template <int NT, int D>
 static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const float* sinks, void* o, float* lse,
                               uint32_t* flags, cudaStream_t st) {
     if (NT == 2) {
         // the register split above is only safe at exactly this launch value
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<NT>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_kernel<NT, D>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     }
-    const size_t smem = sizeof(FwdSmem<NT>) + 1024;
+    const size_t smem = sizeof(FwdSmem<NT, D>) + 1024;
     cudaError_t attr_err = cudaFuncSetAttribute(
-        fwd_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        fwd_tc_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid((P.max_seqlen + kBM - 1) / kBM, P.h_q / NT, P.nseq);
-    fwd_tc_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
-                                                         (__nv_bfloat16*)o, lse, flags);
+    fwd_tc_kernel<NT, D><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
+                                                            (__nv_bfloat16*)o, lse, flags);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -440,12 +484,13 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
                    cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
     CUtensorMap mq, mk, mv;
-    if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM) ||
-        !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
-        !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN))
+    if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM, P.head_dim) ||
+        !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN, P.head_dim) ||
+        !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN, P.head_dim))
         return cudaErrorInvalidValue;
-    if (P.group % 2 == 0) return launch_fwd<2>(P, mq, mk, mv, sinks, o, lse, flags, st);
-    return launch_fwd<1>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    if (P.head_dim == 128) return launch_fwd<1, 128>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    if (P.group % 2 == 0) return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
 }
 
 }  // namespace sinkattn

@@ -55,8 +55,9 @@ def _packed_lengths(seed: int, nseq: int, lo: int, hi: int) -> list:
 
 
 def workload(index: int) -> Workload:
-    """The five workloads: 0 tiny fp32 check; 1 full-causal GPT-OSS-20B layer;
-    2 sliding-window layer; 3 packed variable-length rollouts; 4 long context."""
+    """The workloads: 0 tiny fp32 check; 1 full-causal GPT-OSS-20B layer;
+    2 sliding-window layer; 3 packed variable-length rollouts; 4 long context;
+    5 the same layer with 128-wide heads (half as many)."""
     if index == 0:
         return Workload("tiny_fp32_causal_B1_N128_Hq4_Hkv1_d64", 1, 128, 4, 1, 64, torch.float32,
                         True, 0, seed=0)
@@ -75,6 +76,10 @@ def workload(index: int) -> Workload:
         return Workload("causal_B1_N32768_Hq64_Hkv8_d64_bf16_qk4_sinkU10", 1, 32768, 64, 8, 64,
                         torch.bfloat16, True, 0, seed=4, scale=0.125, qk_gain=4.0,
                         sink_dist="uniform10")
+    if index == 5:
+        # the 128-wide head variant at the same FLOP count as workload 1
+        return Workload("causal_B2_N8192_Hq32_Hkv4_d128_bf16", 2, 8192, 32, 4, 128, torch.bfloat16,
+                        True, 0, seed=5, scale=1.0 / 128 ** 0.5)
     raise ValueError(f"no workload {index}")
 
 

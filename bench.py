@@ -550,7 +550,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=1, help="workload index 0..4")
+    ap.add_argument("--config", type=int, default=1, help="workload index 0..5")
     ap.add_argument("--window", type=int, default=None, help="override the workload's window")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")

@@ -71,7 +71,7 @@ typedef struct CUstream_st* sink_stream_t; /* same object as cudaStream_t; NULL 
 typedef enum {
     SINK_OK = 0,
     SINK_ERR_INVALID_ARG = 1,  /* a NULL/misaligned pointer, a bad size or an inconsistent field */
-    SINK_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim != 64) */
+    SINK_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim not 64 or 128) */
     SINK_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
     SINK_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than sink_attn_workspace_bytes */
     SINK_ERR_TIMEOUT = 5,      /* a kernel's bounded wait gave up (reported by fetch_device_error) */
@@ -87,7 +87,7 @@ typedef struct {
     int total_tokens;     /* T: B * N (padded) or cu_seqlens[batch] (packed) */
     int h_q;              /* query heads; a multiple of h_kv */
     int h_kv;             /* key/value heads */
-    int head_dim;         /* d; 64 is supported */
+    int head_dim;         /* d: 64, or 128 (training entry points only; decode takes 64) */
     sink_dtype_t dtype;   /* dtype of q, k, v, o, dout, dq, dk, dv */
     float softmax_scale;  /* scale applied to Q.K; <= 0 selects 1/sqrt(head_dim) */
     int causal;           /* 1: causal mask; 0: every key of the sequence (window must be 0) */

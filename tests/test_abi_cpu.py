@@ -64,13 +64,17 @@ def test_workspace_sizes(L):
     # the backward holds at least delta [h_q, T] fp32
     assert bwd >= 256 + 4 * 64 * 16384
     assert sa.sink_attn_workspace_bytes(_params(h_q=63), True) == 0
-    assert sa.sink_attn_workspace_bytes(_params(head_dim=128), True) == 0
+    assert sa.sink_attn_workspace_bytes(_params(head_dim=96), True) == 0
+    # head_dim 128: delta and the dS_h partials, no fp32 dQ accumulator (CUDA-core backward)
+    d128 = sa.sink_attn_workspace_bytes(_params(head_dim=128), True)
+    assert 256 + 4 * 64 * 16384 <= d128 < bwd
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(h_q=63), _abi.SINK_ERR_INVALID_ARG),          # h_q not a multiple of h_kv
     (dict(causal=0, window=128), _abi.SINK_ERR_INVALID_ARG),
-    (dict(head_dim=128), _abi.SINK_ERR_UNSUPPORTED),
+    (dict(head_dim=96), _abi.SINK_ERR_UNSUPPORTED),
+    (dict(head_dim=32), _abi.SINK_ERR_UNSUPPORTED),
     (dict(dtype=7), _abi.SINK_ERR_INVALID_ARG),
     (dict(total_tokens=100), _abi.SINK_ERR_INVALID_ARG),  # padded: T != B * N
     (dict(batch=-1), _abi.SINK_ERR_INVALID_ARG),

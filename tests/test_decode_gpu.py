@@ -50,6 +50,8 @@ CASES = [
     ([513, 64], 16, 1),       # group of 16: two query heads per warp
     ([100, 257], 4, 4),       # MHA
     ([300, 77], 32, 1),       # group of 32: the CUDA-core kernel for bf16 too
+    ([77, 1500], 12, 1),      # group of 12: two 8-head blocks, four of them padding
+    ([250, 3], 6, 2),         # group of 3
 ]
 
 

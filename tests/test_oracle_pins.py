@@ -91,6 +91,7 @@ CASES = [
     ([40], 2, 2, 8, True, 5),
     ([12, 25], 6, 3, 8, True, 1),
     ([21], 2, 1, 8, False, 0),
+    ([19, 6], 4, 2, 128, True, 7),   # the 128-wide head of the variants
 ]
 
 

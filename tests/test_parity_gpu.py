@@ -65,6 +65,9 @@ CASES = [
     ([200, 385], 4, 2, True, True, 200),
     ([200], 4, 1, True, False, 0),             # no mask (the page's pseudocode)
     ([5, 0, 7, 130], 4, 2, True, True, 0),     # an empty sequence in the middle
+    ([333, 190], 6, 2, True, True, 0),         # group of 3: the forward's odd-group CTAs
+    ([700], 5, 1, True, True, 4096),           # group of 5, window longer than the sequence
+    ([900, 260], 14, 2, True, True, 640),      # group of 7, window 640
 ]
 
 
@@ -72,6 +75,25 @@ CASES = [
 @pytest.mark.parametrize("lengths,h_q,h_kv,packed,causal,window", CASES)
 def test_small_parity(dtype, lengths, h_q, h_kv, packed, causal, window):
     prob = inputs.random_problem(11, lengths, h_q, h_kv, 64, dtype=dtype, packed=packed,
+                                 sink_scale=2.0)
+    _check(prob, dtype, causal=causal, window=window)
+
+
+D128_CASES = [
+    # lengths, h_q, h_kv, causal, window
+    ([300, 129], 4, 2, True, 0),     # several tiles and ragged tails
+    ([517], 6, 2, True, 200),        # group of 3, window
+    ([200, 1], 2, 1, False, 0),      # no mask
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("lengths,h_q,h_kv,causal,window", D128_CASES)
+def test_head_dim_128_parity(dtype, lengths, h_q, h_kv, causal, window):
+    """head_dim 128: the bf16 forward on the tensor cores (one 128-row tile per
+    CTA, two 64-column atoms per tile), the backward and the fp32 path on the
+    CUDA cores."""
+    prob = inputs.random_problem(21, lengths, h_q, h_kv, 128, dtype=dtype, packed=True,
                                  sink_scale=2.0)
     _check(prob, dtype, causal=causal, window=window)
 
