@@ -188,6 +188,8 @@ sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params, const void* q
     if (tc_bwd_supported(P, bf16))
         e = tc_bwd(P, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace,
                    (char*)workspace + L.tc, s);
+    else if (tc_bwd128_supported(P, bf16))
+        e = tc_bwd128(P, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace, s);
     else
         e = simt_bwd_main(P, bf16, q, k, v, lse, delta, dout, dq, dk, dv, s);
     return cuda_status(e);

@@ -20,4 +20,10 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
                    const float* lse, const float* delta, const void* dout, void* dq, void* dk,
                    void* dv, uint32_t* flags, void* workspace, cudaStream_t st);
 
+// 128-wide heads: a dQ kernel and a dK/dV kernel (tc_bwd128.cu); no workspace.
+bool tc_bwd128_supported(const Problem& P, bool bf16);
+cudaError_t tc_bwd128(const Problem& P, const void* q, const void* k, const void* v,
+                      const float* lse, const float* delta, const void* dout, void* dq, void* dk,
+                      void* dv, uint32_t* flags, cudaStream_t st);
+
 }  // namespace sinkattn
