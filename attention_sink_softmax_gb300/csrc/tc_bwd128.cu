@@ -17,7 +17,7 @@
 //   (tensor-memory lane r), so LSE_r and delta_r are per-thread constants.
 //     S  = Q K^T    A = Q  (tensor memory, written once by the row threads)  TS
 //     dP = dO V^T   A = dO (shared memory, loaded once)                       SS
-//     dQ += dS K    A = dS (tensor memory, from the row threads), B = K MN-major, N = 64 per atom
+//     dQ += dS K    A = dS (tensor memory, from the row threads), B = K MN-major
 //   Tensor memory: S 0..127, dP 128..255, dQ 256..383, dS 384..447, Q 448..511.
 //
 // bwd128_dkdv_kernel: one CTA = 128 keys of one key/value head, walking every
@@ -25,15 +25,17 @@
 //   two warpgroups of elementwise warps split the 128 query rows of a step.
 //     S^T  = K Q^T    A = K (shared memory, loaded once)   SS
 //     dP^T = V dO^T   A = V (shared memory, loaded once)   SS, over S^T once it has been read
-//     dV  += P^T dO   A = P^T  (tensor memory), B = dO MN-major, N = 64 per atom
-//     dK  += dS^T Q   A = dS^T (tensor memory), B = Q  MN-major, N = 64 per atom
+//     dV  += P^T dO   A = P^T  (tensor memory), B = dO MN-major
+//     dK  += dS^T Q   A = dS^T (tensor memory), B = Q  MN-major
 //   The step's LSE and delta rows are staged in shared memory by the producer
 //   warp. Tensor memory: S^T/dP^T 0..127, dV 128..255, dK 256..383, P^T
 //   384..447, dS^T 448..511.
 //
 // Tiles of 128 rows x 128 columns are two 128-byte-swizzled atoms of 64
-// columns, each filled by its own TMA box. dQ, dK and dV are written once, in
-// bf16, with no atomics. Every mbarrier wait is bounded.
+// columns, each filled by its own TMA box. A K-major operand steps through the
+// atoms along K; an MN-major operand (N = 128) spans both, 16 KB apart (the
+// descriptor's leading byte offset). dQ, dK and dV are written once, in bf16,
+// with no atomics. Every mbarrier wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -285,7 +287,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     } else if (lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idSq = idesc_bf16(kB, kB, 0, 0);         // S, dP: B K-major
-        constexpr uint32_t idQ = idesc_bf16(kB, kAtomCols, 0, 1);   // dQ: B = K MN-major
+        constexpr uint32_t idQ = idesc_bf16(kB, kD, 0, 1);          // dQ: B = K MN-major, N = 128
         const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout), 16, 1024);
         auto s_product = [&](int st) {
             const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st]), 16, 1024);
@@ -300,13 +302,10 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 mma_ss(tmem + kColDP, ddo + kstep_off(kk), dv + kstep_off(kk), idSq, kk > 0);
         };
         auto dq_product = [&](int st, bool acc) {
-            const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st]), 1024, 1024);
+            const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[st]), kAtomBytes, 1024);
 #pragma unroll
             for (int kk = 0; kk < kB / 16; ++kk)
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    mma_ts(tmem + kColDQ + a * kAtomCols, tmem + kColDS + kk * 8, dk + mnstep_off(a, kk),
-                           idQ, acc || kk > 0);
+                mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, dk + mnstep_off(0, kk), idQ, acc || kk > 0);
         };
         bool ok = wait_phase(&sm.q_ready, 0, flags, abort_word) &&
                   wait_phase(&sm.k_full[0], 0, flags, abort_word);
@@ -587,7 +586,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     } else if (lane == 0) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idS = idesc_bf16(kB, kB, 0, 0);         // S^T, dP^T: A, B K-major
-        constexpr uint32_t idG = idesc_bf16(kB, kAtomCols, 0, 1);  // dV, dK: B MN-major
+        constexpr uint32_t idG = idesc_bf16(kB, kD, 0, 1);         // dV, dK: B MN-major, N = 128
         const uint64_t dkey = smem_desc_sw128(smem_u32(sm.k), 16, 1024);
         const uint64_t dval = smem_desc_sw128(smem_u32(sm.v), 16, 1024);
         auto st_product = [&](int st) {
@@ -603,20 +602,14 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mma_ss(tmem + kColSP, dval + kstep_off(kk), ddo + kstep_off(kk), idS, kk > 0);
         };
         auto grads = [&](int st, bool acc) {
-            const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), 1024, 1024);
-            const uint64_t dqm = smem_desc_sw128(smem_u32(sm.q[st]), 1024, 1024);
+            const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), kAtomBytes, 1024);
+            const uint64_t dqm = smem_desc_sw128(smem_u32(sm.q[st]), kAtomBytes, 1024);
 #pragma unroll
             for (int kk = 0; kk < kB / 16; ++kk)
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    mma_ts(tmem + kColDV + a * kAtomCols, tmem + kColPT + kk * 8, ddo + mnstep_off(a, kk),
-                           idG, acc || kk > 0);
+                mma_ts(tmem + kColDV, tmem + kColPT + kk * 8, ddo + mnstep_off(0, kk), idG, acc || kk > 0);
 #pragma unroll
             for (int kk = 0; kk < kB / 16; ++kk)
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    mma_ts(tmem + kColDK + a * kAtomCols, tmem + kColDST + kk * 8, dqm + mnstep_off(a, kk),
-                           idG, acc || kk > 0);
+                mma_ts(tmem + kColDK, tmem + kColDST + kk * 8, dqm + mnstep_off(0, kk), idG, acc || kk > 0);
         };
         bool ok = wait_phase(&sm.kv_full, 0, flags, abort_word) &&
                   wait_phase(&sm.q_full[0], 0, flags, abort_word);

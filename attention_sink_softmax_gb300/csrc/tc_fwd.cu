@@ -33,7 +33,7 @@
 //
 // Head dim D = 64 or 128. A tile of D columns is held as D/64 swizzle atoms
 // of 128 rows x 64 (128-byte rows), each filled by its own TMA box; S takes
-// D/16 K steps across the atoms, and P V is issued per atom (N = 64 each).
+// D/16 K steps across the atoms, and P V is one N = D product per K step.
 // At D = 128 a CTA holds one tile (NT = 1): S 128 + O 128 + P 64 columns.
 #include <cudaTypedefs.h>
 
@@ -344,7 +344,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // ------------------------------------------------------------ MMA issuer of tile t
             const int t = warp - (4 * NT + 1);
             constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);       // Q, K both K-major
-            constexpr uint32_t idO = idesc_bf16(kBM, kAtomCols, 0, 1);  // P from TMEM, V MN-major
+            // P from TMEM, V MN-major with N = D: at D = 128 the two 64-column
+            // atoms are 16 KB apart (the descriptor's leading byte offset)
+            constexpr uint32_t idO = idesc_bf16(kBM, D, 0, 1);
             const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
             // K step kk of S reads atom kk / 4 at byte offset 32 (kk % 4); both are
             // added to the descriptors' start-address field (16-byte units)
@@ -380,14 +382,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
                 if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
                 tc_fence_after();
-                const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), 1024, 1024);
+                const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), kAtomBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-#pragma unroll
-                    for (int a = 0; a < kAtoms; ++a)
-                        mma_ts(tO + a * kAtomCols, tP + kk * 8,
-                               dv + (uint64_t)((a * kAtomBytes + kk * 16 * 128) >> 4), idO,
-                               (i > 0 || kk > 0));
+                    mma_ts(tO, tP + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
                 mma_commit(&sm.o_done[t]);
                 // this tile's last reads of stage st (K(i) by S_t(i), V(i) by the product above)
                 mma_commit(&sm.kv_empty[st]);
