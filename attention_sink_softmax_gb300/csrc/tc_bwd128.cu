@@ -363,8 +363,8 @@ struct DkvSmem {
     alignas(1024) __nv_bfloat16 v[kB * kD];
     alignas(1024) __nv_bfloat16 q[kBStages][kB * kD];
     alignas(1024) __nv_bfloat16 dout[kBStages][kB * kD];
-    float lse2[kBStages][kB];  // LSE * log2 e of the step's rows (0 past the sequence)
-    float dlt[kBStages][kB];   // delta of the step's rows
+    alignas(16) float lse2[kBStages][kB];  // LSE * log2 e of the step's rows (0 past the sequence)
+    alignas(16) float dlt[kBStages][kB];   // delta of the step's rows
     uint64_t kv_full;
     uint64_t q_full[kBStages], q_empty[kBStages], rows_full[kBStages];
     uint64_t s_full, s_loaded, dp_full, dp_loaded, ds_full, pd_free, acc_done, drained;
@@ -446,15 +446,22 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&sm.s_loaded);  // dP^T may be written over S^T
-                const float* l2 = sm.lse2[st] + g * 64;
+                // the rows' LSE as 16-byte broadcast loads (every lane reads the same row values)
+                const float4* l4 = reinterpret_cast<const float4*>(sm.lse2[st] + g * 64);
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float x0, x1;
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 l = l4[c / 4];
+                    float x0, x1, x2, x3;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(a[c]), __uint_as_float(a[c + 1])), sc2,
-                                     f2_pack(-l2[c], -l2[c + 1])),
+                                     f2_pack(-l.x, -l.y)),
                               x0, x1);
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(a[c + 2]), __uint_as_float(a[c + 3])), sc2,
+                                     f2_pack(-l.z, -l.w)),
+                              x2, x3);
                     p[c] = fast_exp2(x0);
                     p[c + 1] = fast_exp2(x1);
+                    p[c + 2] = fast_exp2(x2);
+                    p[c + 3] = fast_exp2(x3);
                 }
             }
             // rows that do not see this key (causal diagonal block, window edge,
@@ -481,13 +488,16 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive(&sm.dp_loaded);  // the next step's S^T may be issued
-                const float* dl = sm.dlt[st] + g * 64;
+                const float4* d4 = reinterpret_cast<const float4*>(sm.dlt[st] + g * 64);
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    const float ds0 = p[c] * (__uint_as_float(d[c]) - dl[c]);
-                    const float ds1 = p[c + 1] * (__uint_as_float(d[c + 1]) - dl[c + 1]);
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 dl = d4[c / 4];
                     pw[c / 2] = pack_bf16x2(p[c], p[c + 1]);
-                    dw[c / 2] = pack_bf16x2(ds0, ds1);
+                    pw[c / 2 + 1] = pack_bf16x2(p[c + 2], p[c + 3]);
+                    dw[c / 2] = pack_bf16x2(p[c] * (__uint_as_float(d[c]) - dl.x),
+                                            p[c + 1] * (__uint_as_float(d[c + 1]) - dl.y));
+                    dw[c / 2 + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(d[c + 2]) - dl.z),
+                                                p[c + 3] * (__uint_as_float(d[c + 3]) - dl.w));
                 }
             }
             if (i > 0) {
