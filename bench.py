@@ -219,6 +219,7 @@ KERNEL_SOURCES = {
     "bwd_main": ["common.cuh", "tc.h", "tc_bwd.cu", "tc_common.cuh", "tc_ptx.cuh"],
     "fwd": ["common.cuh", "tc.h", "tc_fwd.cu", "tc_common.cuh", "tc_ptx.cuh"],
     "decode": ["common.cuh", "decode.cu", "tc_common.cuh", "tc_ptx.cuh"],
+    "bwd_main_d128": ["common.cuh", "tc.h", "tc_bwd128.cu", "tc_common.cuh", "tc_ptx.cuh"],
 }
 
 
@@ -426,7 +427,10 @@ def run_gpu(args, w, window):
     # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop
     main_ms = stage_ms[2]
     main_tflops = f_bwd / (main_ms / 1000) / 1e12
-    traffic = profiled_traffic(kernel_sources("bwd_main"), "bwd_main")
+    # the 64-wide backward is one kernel; at d = 128 it is the dQ and dK/dV kernels
+    # (their traffic entry is the sum of one launch of each)
+    stage = "bwd_main" if w.head_dim == 64 else "bwd_main_d128"
+    traffic = profiled_traffic(kernel_sources(stage), stage) if stage in KERNEL_SOURCES else None
     roofline = {"bound": "tensor", "achieved": main_tflops,
                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
