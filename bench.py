@@ -61,6 +61,22 @@ def flops_of(w, window):
     return 4 * w.head_dim * p, 10 * w.head_dim * p
 
 
+def bytes_of(w) -> dict:
+    """Algorithmic bytes per step (each tensor read or written once):
+    forward reads Q, K, V and writes O and LSE; the preprocess reads O, dO and
+    LSE and writes D; the backward main reads Q, K, V, dO, LSE and D and writes
+    dQ, dK and dV. The fp32 dQ accumulator is implementation traffic, not
+    counted."""
+    T = w.total_tokens
+    e = 2 if w.dtype == torch.bfloat16 else 4
+    q = T * w.h_q * w.head_dim * e   # Q, O, dO, dQ each
+    kv = T * w.h_kv * w.head_dim * e  # K, V, dK, dV each
+    row = 4 * w.h_q * T               # LSE or D (fp32)
+    return {"fwd": q + 2 * kv + q + row,
+            "bwd_preprocess": 2 * q + row + row,
+            "bwd_main": q + 2 * kv + q + 2 * row + q + 2 * kv}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -424,17 +440,38 @@ def run_gpu(args, w, window):
                       dk, dv, dsinks, work, flops_step)
 
     pk, pk_src = peaks()
-    # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop
+    # per-stage rates: FLOP/s (backward also without the S recompute, 8 d per
+    # pair) and algorithmic bytes/s
+    nbytes = bytes_of(w)
+    f_bwd_norecompute = f_bwd * 8 // 10
+    names = ("fwd", "bwd_preprocess", "bwd_main")
+    stage_rates = {n: {"gb_per_s": nbytes[n] / (stage_ms[j] / 1000) / 1e9} for j, n in enumerate(names)}
+    stage_rates["fwd"]["tflops"] = f_fwd / (stage_ms[0] / 1000) / 1e12
+    bwd_ms = stage_ms[1] + stage_ms[2]
+    stage_rates["bwd"] = {"tflops": f_bwd / (bwd_ms / 1000) / 1e12,
+                          "tflops_no_recompute": f_bwd_norecompute / (bwd_ms / 1000) / 1e12,
+                          "gb_per_s": (nbytes["bwd_preprocess"] + nbytes["bwd_main"]) / (bwd_ms / 1000) / 1e9}
+    # dominant stage: the backward main loop (sink_attn_bwd_main), timed inside the step loop.
+    # It is tensor-bound unless its arithmetic intensity is below the ridge point
+    # (the short-window layers), then HBM-bound.
     main_ms = stage_ms[2]
     main_tflops = f_bwd / (main_ms / 1000) / 1e12
     # the 64-wide backward is one kernel; at d = 128 it is the dQ and dK/dV kernels
     # (their traffic entry is the sum of one launch of each)
     stage = "bwd_main" if w.head_dim == 64 else "bwd_main_d128"
     traffic = profiled_traffic(kernel_sources(stage), stage) if stage in KERNEL_SOURCES else None
-    roofline = {"bound": "tensor", "achieved": main_tflops,
-                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
-                "kernel": "sink_attn_bwd_main", "peak_kind": f"bf16 sustained ({pk_src})"}
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if f_bwd / nbytes["bwd_main"] >= ridge:
+        roofline = {"bound": "tensor", "achieved": main_tflops,
+                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
+                    "kernel": "sink_attn_bwd_main", "peak_kind": f"bf16 sustained ({pk_src})"}
+    else:
+        main_gbs = stage_rates["bwd_main"]["gb_per_s"]
+        roofline = {"bound": "hbm", "achieved": main_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": main_gbs / pk["hbm_gbs"], "traffic": traffic,
+                    "kernel": "sink_attn_bwd_main", "peak_kind": f"HBM copy ({pk_src})",
+                    "algorithmic_bytes": nbytes["bwd_main"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -446,6 +483,7 @@ def run_gpu(args, w, window):
                         "sustained": 100 * value / ws / pk["bf16_tflops_sustained"],
                         "source": pk_src},
         "stages_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1], "bwd_main": stage_ms[2]},
+        "stage_rates": stage_rates,
         "clocks": clk.summary(),
         "e2e": e2e,
         "gpu_launches": int(launches),

@@ -84,3 +84,19 @@ def test_reference_arm_line_matches_gpu_arm_config(monkeypatch, capsys):
     assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_algorithmic_bytes_and_flops_of_the_target_layer():
+    """Per-stage algorithmic bytes and FLOPs of the causal B=2 N=8192 64/8 d=64
+    layer: forward reads Q, K, V and writes O, LSE (306 MB); the preprocess
+    reads O, dO, LSE and writes D (277 MB); 4.295e9 unmasked pairs."""
+    w = inputs.workload(1)
+    b = bench.bytes_of(w)
+    assert b["fwd"] == 2 * 16384 * 64 * 64 * 2 + 2 * 16384 * 8 * 64 * 2 + 4 * 64 * 16384
+    assert round(b["fwd"] / 1e6) == 306 and round(b["bwd_preprocess"] / 1e6) == 277
+    assert bench.pairs_of(w, 0) == 2 * 64 * 8192 * 8193 // 2
+    f_fwd, f_bwd = bench.flops_of(w, 0)
+    assert f_fwd == 4 * 64 * bench.pairs_of(w, 0) and f_bwd == 10 * 64 * bench.pairs_of(w, 0)
+    # the window-128 layer's backward sits below the ridge point: HBM-bound
+    w2 = inputs.workload(2)
+    assert bench.flops_of(w2, 128)[1] / bench.bytes_of(w2)["bwd_main"] < 1749.9e12 / 6796.9e9
