@@ -40,7 +40,8 @@
  * workspace (size from sink_attn_workspace_bytes). No entry point allocates,
  * frees or synchronises except sink_attn_fetch_device_error, which says so.
  * Work is enqueued on the caller's stream; outputs are valid once that stream
- * reaches the enqueued work. Outputs (o, lse, dq, dk, dv, dsinks) are
+ * reaches the enqueued work, so every other entry point may be captured in a
+ * CUDA graph and replayed. Outputs (o, lse, dq, dk, dv, dsinks) are
  * overwritten, never accumulated into. Inputs are not modified.
  *
  * Errors. Every entry point returns a status. Arguments are validated before
@@ -112,8 +113,12 @@ SINK_API sink_status_t sink_attn_fwd(const sink_attn_params_t* params,
  * upstream gradient dout, writes dq (input dtype), dk, dv (input dtype, summed
  * over the query heads of each key/value head) and dsinks (fp32 [h_q],
  * dL/dS_h summed over every sequence and row of head h, reduced in a fixed
- * order so it is bitwise reproducible). Equivalent to sink_attn_bwd_preprocess
- * into workspace followed by sink_attn_bwd_main. */
+ * order so it is bitwise reproducible). dk, dv and dsinks are bitwise
+ * reproducible; dq on the bf16 d = 64 path is summed over key blocks by fp32
+ * reduce-adds into the workspace in an order that varies between runs, so it
+ * may differ in the last bf16 place (at d = 128 and in fp32 it is
+ * reproducible). Equivalent to sink_attn_bwd_preprocess into workspace
+ * followed by sink_attn_bwd_main. */
 SINK_API sink_status_t sink_attn_bwd(const sink_attn_params_t* params,
                             const void* q, const void* k, const void* v,
                             const float* sinks, const int32_t* cu_seqlens,
