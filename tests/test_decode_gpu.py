@@ -190,3 +190,27 @@ def test_decode_under_cuda_graph_capture_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(o_g, o_e) and torch.equal(lse_g, lse_e)
     assert sa.sink_attn_fetch_device_error(ws)[0] == _abi.SINK_OK
+
+
+def test_decode_empty_batch_and_empty_cache():
+    """No query: nothing is enqueued and the call succeeds. An empty cache:
+    every context is invalid, so every query gets the empty row (o = 0,
+    lse = S_h) and the flag word reports it."""
+    sinks = torch.randn(8).float().to(DEV)
+    k = torch.randn(10, 2, 64).bfloat16().to(DEV)
+    q0 = torch.empty(0, 8, 64, dtype=torch.bfloat16, device=DEV)
+    z = torch.empty(0, dtype=torch.int32, device=DEV)
+    o, lse = sa.sink_attn_decode(q0, k, k, sinks, z, z, max_seqlen=10)
+    torch.cuda.synchronize()
+    assert o.shape == (0, 8, 64) and lse.shape == (8, 0)
+    q = torch.randn(2, 8, 64).bfloat16().to(DEV)
+    k0 = torch.empty(0, 2, 64, dtype=torch.bfloat16, device=DEV)
+    starts = torch.zeros(2, dtype=torch.int32, device=DEV)
+    lens = torch.ones(2, dtype=torch.int32, device=DEV)
+    p = sa.make_decode_params(q, k0, max_seqlen=4)
+    ws = torch.empty(sa.sink_attn_decode_workspace_bytes(p), dtype=torch.uint8, device=DEV)
+    o, lse = sa.sink_attn_decode(q, k0, k0, sinks, starts, lens, params=p, workspace=ws)
+    st, flags = sa.sink_attn_fetch_device_error(ws)
+    assert st == _abi.SINK_ERR_DEVICE and flags != 0
+    assert torch.all(o.float() == 0)
+    torch.testing.assert_close(lse, sinks[:, None].expand(8, 2), rtol=1e-6, atol=1e-6)
