@@ -269,6 +269,32 @@ def test_window_one_is_diagonal_sigmoid_and_wide_window_is_causal():
         np.testing.assert_array_equal(a, b)
 
 
+@pytest.mark.parametrize("c", [7.5, -40.0])
+def test_adding_a_constant_to_every_logit_of_a_row_changes_only_the_lse(c):
+    """Softmax shift invariance at the logit level (section "数学公式深入解读":
+    P_ij and P_{i,h} share one denominator): a column c / scale appended to Q
+    against a column of ones appended to K adds c to every score, and c is
+    added to S_h; then O and P_sink (hence dS_h) are unchanged and LSE grows by
+    exactly c."""
+    rng = np.random.default_rng(31)
+    q, k, v, sinks, dout = _rand_problem(rng, 23, 4, 2, 8)
+    cu = np.array([0, 9, 23], np.int32)
+    kw = dict(scale=0.3, causal=True, window=0, cu_seqlens=cu)
+    o, lse = oracle.forward(q, k, v, sinks, **kw)
+    ds = oracle.backward(q, k, v, sinks, dout, **kw)[3]
+
+    def extend(x, value):
+        return np.concatenate([x, np.full(x.shape[:2] + (1,), value)], axis=2)
+
+    q2, k2, v2, dout2 = extend(q, c / 0.3), extend(k, 1.0), extend(v, 0.0), extend(dout, 0.0)
+    o2, lse2 = oracle.forward(q2, k2, v2, sinks + c, **kw)
+    ds2 = oracle.backward(q2, k2, v2, sinks + c, dout2, **kw)[3]
+    np.testing.assert_allclose(o2[..., :8], o, rtol=0, atol=1e-12)
+    assert np.all(o2[..., 8] == 0)
+    np.testing.assert_allclose(lse2, lse + c, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ds2, ds, rtol=0, atol=1e-11)
+
+
 def test_gqa_equals_mha_with_repeated_kv():
     rng = np.random.default_rng(31)
     T, h_q, h_kv, d = 19, 6, 2, 8
