@@ -54,6 +54,8 @@ def _pin_calls():
     calls.append((pins.test_window_one_is_diagonal_sigmoid_and_wide_window_is_causal, ()))
     calls.append((pins.test_gqa_equals_mha_with_repeated_kv, ()))
     calls.append((pins.test_hand_worked_example_fixture, ()))
+    calls.append((pins.test_adding_a_constant_to_every_logit_of_a_row_changes_only_the_lse, (7.5,)))
+    calls.append((pins.test_decode_window_one_is_a_sigmoid_of_the_newest_key, ()))
     return calls
 
 
