@@ -9,8 +9,18 @@ of Q/K/V/dO) exceed the 129 MB L2, so no extra flush is done between steps.
 FLOP convention (algorithmic, unmasked (row, key) pairs only): forward 4*d per
 pair (QK^T and PV), backward 10*d per pair (QK^T recompute, dP, dV, dK, dQ).
 
+The line also carries: ``stage_rates`` (per-stage TFLOP/s and algorithmic
+GB/s, the backward also without the recompute), ``roofline`` for the dominant
+stage (the backward main loop; against HBM when its arithmetic intensity is
+below the ridge point, as in the window layers), ``e2e`` (the same step with
+inputs copied in from pinned host memory and every output copied back each
+step, the copies overlapping the neighbouring steps' compute), ``clocks``
+sampled during the timed region and ``cpu_baseline`` (the oracle on the host
+cores, bounded sample).
+
 Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
 instead (the only reference this method has), on a bounded sample.
+``--decode`` prints a separate line for the decode path (KV-cache bandwidth).
 """
 from __future__ import annotations
 
