@@ -403,6 +403,406 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
+// ---------------------------------------------------------------- several row tiles per CTA
+// A short window (at most 256 keys) leaves each row tile one or two key
+// blocks, too little work to hide a CTA's start-up (tensor-memory allocation,
+// first loads, pipeline fill) and its epilogue. fwd_tc_tiles_kernel runs
+// kWindowTiles consecutive row tiles of the same query heads in one CTA: the
+// next tile's Q is loaded into the second Q buffer while the current tile
+// computes, the K/V ring and the barrier phases run on across tiles (a block
+// counter g), and each tile's first P V waits until the softmax has read the
+// previous tile's O (o_free). It is the kernel above generalised to several
+// tiles; the one-tile kernel is kept separate because the generalised loops
+// cost it about 7 % on the causal layer. d = 64 only.
+constexpr int kWindowTiles = 4;
+
+template <int NT>
+struct FwdTilesSmem {
+    alignas(1024) __nv_bfloat16 q[2][NT][kBM * 64];
+    alignas(1024) __nv_bfloat16 k[kStages][kBN * 64];
+    alignas(1024) __nv_bfloat16 v[kStages][kBN * 64];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
+    uint64_t o_free[NT];    // the softmax has read O_t of its tile: the next tile may overwrite it
+    uint64_t exp_turn[NT];  // the two tiles' exponentials take turns (NT = 2)
+    uint64_t drained[NT];
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+static_assert(sizeof(FwdTilesSmem<2>) + 1024 <= 232448, "shared memory of the multi-tile forward");
+
+template <int NT>
+__global__ void __launch_bounds__(fwd_threads<NT>(), 1)
+fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const Problem P,
+              const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
+              float* __restrict__ lse, uint32_t* flags) {
+    constexpr int D = 64;
+    constexpr int kTiles = kWindowTiles;
+    constexpr int kQBufs = 2;
+    constexpr int kAtoms = D / kAtomCols;
+    constexpr uint32_t kTileBytes = tile_bytes<D>();
+    extern __shared__ uint8_t smem_raw[];
+    FwdTilesSmem<NT>& sm = *reinterpret_cast<FwdTilesSmem<NT>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int cb = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+    const int seq = blockIdx.z;
+    const int h0 = blockIdx.y * NT;
+    int start, L;
+    seq_bounds(P, seq, start, L);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && L > P.max_seqlen) atomicOr(flags, kFlagSeqTooLong);
+    // this CTA's row tiles: row blocks rb0 .. rb0 + ntile - 1 of the sequence
+    const int rb0 = cb * kTiles;
+    const int ntile = kTiles == 1 ? 1 : min(kTiles, (L + kBM - 1) / kBM - rb0);
+    if (rb0 * kBM >= L) return;  // uniform for the whole CTA, before any barrier or TMEM use
+    // first row, first key block and number of key blocks of tile k
+    auto tile_blocks = [&](int k, int& r0, int& kb_lo, int& nblk) {
+        const int rb = rb0 + k;
+        r0 = rb * kBM;
+        kb_lo = 0;
+        int kb_hi = (L - 1) / kBN;
+        if (P.causal) {
+            kb_hi = rb;
+            if (P.window > 0) kb_lo = max(0, r0 - P.window + 1) / kBN;
+        }
+        nblk = kb_hi - kb_lo + 1;
+    };
+    const int hk = h0 / P.group;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kQBufs; ++b) {
+            mbar_init(&sm.q_full[b], 1);
+            mbar_init(&sm.q_empty[b], NT);  // one commit from each tile's MMA issuer
+        }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.kv_empty[i], NT);  // one commit from each tile's MMA issuer
+        }
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.s_loaded[t], 128);
+            mbar_init(&sm.p_full[t], 128);
+            mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.exp_turn[t], 128);
+            mbar_init(&sm.o_free[t], 128);
+        }
+        for (int t = 0; t < NT; ++t) mbar_init(&sm.drained[t], 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc<512>(&sm.tmem_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_slot;
+    volatile int* abort_word = &sm.abort_flag;
+
+    if (warp < 4 * NT) {
+        if (NT == 2) regs_increase<kSoftmaxRegs>();
+        // ------------------------------------------------------------ softmax warpgroup t
+        const int t = warp / 4;
+        const int wq = warp % 4;
+        const int r = wq * 32 + lane;
+        const int h = h0 + t;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * 64;
+        const uint32_t tP = tmem + lane_off + 384 + t * 64;
+        const float sc = P.scale_log2;
+        const float sink2 = __ldg(sinks + h) * kLog2e;
+        bool ok = true;
+        int g = 0;  // key blocks of this CTA so far: the barrier phases run on across its tiles
+        for (int k = 0; ok && k < ntile; ++k) {
+        int r0, kb_lo, nblk;
+        tile_blocks(k, r0, kb_lo, nblk);
+        const int row = r0 + r;
+        const bool valid = row < L;
+        float m = sink2;                       // running max in log2 units, seeded by the sink
+        float l = m == -INFINITY ? 0.f : 1.f;  // running sum, seeded by the sink's own term
+        for (int i = 0; i < nblk; ++i, ++g) {
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], g & 1, flags, abort_word));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+            {
+                uint32_t a[128];
+                tmem_ld128(tS, a);
+                tmem_ld_wait();
+                // S_t is in registers: the next block's S_t product may be issued
+                tc_fence_before();
+                mbar_arrive(&sm.s_loaded[t]);
+#pragma unroll
+                for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(a[j]);
+            }
+            const int kp0 = (kb_lo + i) * kBN;  // first key position of the block
+            const bool need_mask =
+                P.causal ? (kp0 + kBN - 1 > r0 ||
+                            (P.window > 0 && kp0 < r0 + kBM - P.window))
+                         : (kp0 + kBN > L);
+            if (need_mask) {
+                const int lo = P.causal && P.window > 0 ? row - P.window + 1 : INT_MIN;
+                const int hi = P.causal ? min(row, L - 1) : L - 1;
+#pragma unroll
+                for (int j = 0; j < 128; ++j) {
+                    const int kp = kp0 + j;
+                    if (kp < lo || kp > hi) s[j] = -INFINITY;
+                }
+            }
+            // row max: three-input max, four independent chains
+            float mx4[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
+#pragma unroll
+            for (int j = 8; j < 128; j += 8) {
+                mx4[0] = max3f(mx4[0], s[j], s[j + 1]);
+                mx4[1] = max3f(mx4[1], s[j + 2], s[j + 3]);
+                mx4[2] = max3f(mx4[2], s[j + 4], s[j + 5]);
+                mx4[3] = max3f(mx4[3], s[j + 6], s[j + 7]);
+            }
+            const float smax = max3f(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
+            const float mx = smax * sc;
+            const bool upd = i == 0 ? mx > m : mx > m + kRescaleLog2;
+            const float m_new = upd ? mx : m;
+            const float corr = upd ? (m == -INFINITY ? 0.f : fast_exp2(m - m_new)) : 1.f;
+            const float mref = m_new == -INFINITY ? 0.f : m_new;
+            // p = exp2(s * sc - mref), two columns per paired op; row sum in pairs
+            const uint64_t sc2 = f2_pack(sc, sc);
+            const uint64_t nm2 = f2_pack(-mref, -mref);
+            uint64_t rs2[4] = {0, 0, 0, 0};
+            // With two tiles the exponentials alternate (tile 0 block i, tile 1 block
+            // i, tile 0 block i+1, ...), so one tile's exp2 loop overlaps the other
+            // tile's loads, max and stores instead of both competing for the
+            // special-function units at once.
+            if (NT == 2 && (t == 1 || g > 0)) {
+                const int ph = t == 0 ? g - 1 : g;
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word));
+                if (!ok) break;
+            }
+            // P into registers first (bf16 pairs): the exponentials overlap the
+            // previous block's P V product, which still reads P_t and writes O_t
+            uint32_t pk[64];
+#pragma unroll
+            for (int j = 0; j < 128; j += 2) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[j], s[j + 1]), sc2, nm2), x0, x1);
+                const float p0 = fast_exp2(x0);
+                const float p1 = fast_exp2(x1);
+                rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
+                pk[j >> 1] = pack_bf16x2(p0, p1);
+            }
+            if (NT == 2) mbar_arrive(&sm.exp_turn[(1 - t) % NT]);
+            if (g > 0) {
+                // P_t V of the previous block (possibly the previous tile's) is done with P_t
+                ok = __all_sync(0xffffffffu,
+                                wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st64(tP, pk);
+            float r0, r1, r2, r3, r4, r5, r6, r7;
+            f2_unpack(rs2[0], r0, r1);
+            f2_unpack(rs2[1], r2, r3);
+            f2_unpack(rs2[2], r4, r5);
+            f2_unpack(rs2[3], r6, r7);
+            const float rs = ((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7));
+            if (i > 0 && __any_sync(0xffffffffu, upd)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 64) {
+                    uint32_t oa[32], ob[32];
+                    tmem_ld32(tO + c0, oa);
+                    tmem_ld32(tO + c0 + 32, ob);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        oa[j] = __float_as_uint(__uint_as_float(oa[j]) * corr);
+                        ob[j] = __float_as_uint(__uint_as_float(ob[j]) * corr);
+                    }
+                    tmem_st32(tO + c0, oa);
+                    tmem_st32(tO + c0 + 32, ob);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[t]);
+            l = l * corr + rs;
+            m = m_new;
+        }
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word));
+        if (!ok) break;
+        {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * D);
+            uint32_t o_all[D];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t oa[32];
+                tmem_ld32(tO + c0, oa);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o_all[c0 + j] = oa[j];
+            }
+            tmem_ld_wait();
+            // O_t is in registers: the next tile's first P V may overwrite it
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[t]);
+            if (valid) {
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(o_all[8 * j + 0]) * inv, __uint_as_float(o_all[8 * j + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o_all[8 * j + 2]) * inv, __uint_as_float(o_all[8 * j + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o_all[8 * j + 4]) * inv, __uint_as_float(o_all[8 * j + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o_all[8 * j + 6]) * inv, __uint_as_float(o_all[8 * j + 7]) * inv);
+                    dst[j] = w;
+                }
+                lse[(size_t)h * P.total + start + row] = (m + __log2f(l)) * kLn2;
+            }
+        }
+        }  // tiles
+        } else {
+        if (NT == 2) regs_decrease<kOtherRegs>();
+        if (warp == 4 * NT) {
+            // ------------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+                int g = 0, issued = 0, q_issued = 0;
+                bool ok = true;
+                for (int k = 0; ok && k < ntile; ++k) {
+                    int r0, kb_lo, nblk;
+                    tile_blocks(k, r0, kb_lo, nblk);
+                    const int qb = k % kQBufs;
+                    // the buffer's previous tile: every S product that read it has completed
+                    if (k >= kQBufs &&
+                        !wait_phase(&sm.q_empty[qb], ((k / kQBufs) - 1) & 1, flags, abort_word))
+                        break;
+                    mbar_arrive_expect_tx(&sm.q_full[qb], NT * kTileBytes);
+                    for (int t = 0; t < NT; ++t)
+                        for (int a = 0; a < kAtoms; ++a)
+                            tma_load_3d(sm.q[qb][t] + a * kBM * kAtomCols, &tmQ, &sm.q_full[qb],
+                                        a * kAtomCols, h0 + t, start + r0);
+                    q_issued = k + 1;
+                    for (int i = 0; i < nblk; ++i, ++g) {
+                        const int st = g % kStages;
+                        if (g >= kStages &&
+                            !wait_phase(&sm.kv_empty[st], ((g / kStages) - 1) & 1, flags, abort_word)) {
+                            ok = false;
+                            break;
+                        }
+                        const int kpos = start + (kb_lo + i) * kBN;
+                        mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                        for (int a = 0; a < kAtoms; ++a)
+                            tma_load_3d(sm.k[st] + a * kBN * kAtomCols, &tmK, &sm.k_full[st], a * kAtomCols,
+                                        hk, kpos);
+                        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                        for (int a = 0; a < kAtoms; ++a)
+                            tma_load_3d(sm.v[st] + a * kBN * kAtomCols, &tmV, &sm.v_full[st], a * kAtomCols,
+                                        hk, kpos);
+                        issued = g + 1;
+                    }
+                }
+                // copies still in flight must land before the CTA's shared memory goes away
+                for (int k = max(0, q_issued - kQBufs); k < q_issued; ++k)
+                    drain_phase(&sm.q_full[k % kQBufs], (k / kQBufs) & 1);
+                for (int j = max(0, issued - kStages); j < issued; ++j) {
+                    const int st = j % kStages;
+                    drain_phase(&sm.k_full[st], (j / kStages) & 1);
+                    drain_phase(&sm.v_full[st], (j / kStages) & 1);
+                }
+            }
+        } else if (warp >= 4 * NT + 1 && warp <= 4 * NT + NT && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer of tile t
+            const int t = warp - (4 * NT + 1);
+            constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);       // Q, K both K-major
+            // P from TMEM, V MN-major with N = D: at D = 128 the two 64-column
+            // atoms are 16 KB apart (the descriptor's leading byte offset)
+            constexpr uint32_t idO = idesc_bf16(kBM, D, 0, 1);
+            const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
+            // S_t = Q_t K^T from Q buffer qb and K stage st. K step kk reads atom
+            // kk / 4 at byte offset 32 (kk % 4); both are added to the
+            // descriptors' start-address field (16-byte units)
+            const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q[0][t]), 16, 1024);
+            const uint64_t dq1 = smem_desc_sw128(smem_u32(sm.q[kQBufs - 1][t]), 16, 1024);
+            auto s_product = [&](int qb, int stage) {
+                const uint64_t dq = qb == 0 ? dq0 : dq1;
+                const uint64_t dk = smem_desc_sw128(smem_u32(sm.k[stage]), 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk / 4) * kAtomBytes) >> 4) + 2 * (kk % 4);
+                    mma_ss(tS, dq + off, dk + off, idS, kk > 0);
+                }
+            };
+            int r0, kb_lo, nblk;
+            tile_blocks(0, r0, kb_lo, nblk);
+            bool ok = wait_phase(&sm.q_full[0], 0, flags, abort_word) &&
+                      wait_phase(&sm.k_full[0], 0, flags, abort_word);
+            if (ok) {
+                tc_fence_after();
+                s_product(0, 0);
+                mma_commit(&sm.s_full[t]);
+                if (nblk == 1) mma_commit(&sm.q_empty[0]);  // the tile's only S product
+            }
+            int g = 0;
+            for (int k = 0; ok && k < ntile; ++k) {
+                tile_blocks(k, r0, kb_lo, nblk);
+                const int qb = k % kQBufs;
+                for (int i = 0; i < nblk; ++i, ++g) {
+                    const int st = g % kStages;
+                    const int st1 = (g + 1) % kStages;
+                    // S_t of the next block (of this tile, or the first of the next tile)
+                    // as soon as S_t of this block has been read
+                    const bool next_here = i + 1 < nblk;
+                    if (next_here || k + 1 < ntile) {
+                        if (!(ok = wait_phase(&sm.s_loaded[t], g & 1, flags, abort_word))) break;
+                        int nqb = qb, last_of_tile = i + 2 == nblk;
+                        if (!next_here) {
+                            int nr0, nkb_lo, nnblk;
+                            tile_blocks(k + 1, nr0, nkb_lo, nnblk);
+                            nqb = (k + 1) % kQBufs;
+                            last_of_tile = nnblk == 1;
+                            if (!(ok = wait_phase(&sm.q_full[nqb], ((k + 1) / kQBufs) & 1, flags, abort_word)))
+                                break;
+                        }
+                        if (!(ok = wait_phase(&sm.k_full[st1], ((g + 1) / kStages) & 1, flags, abort_word)))
+                            break;
+                        tc_fence_after();
+                        s_product(nqb, st1);
+                        mma_commit(&sm.s_full[t]);
+                        // the last S product of a tile frees its Q buffer once it completes
+                        if (last_of_tile) mma_commit(&sm.q_empty[nqb]);
+                    }
+                    // O_t += P_t(g) V(g); the first block of a tile overwrites O_t,
+                    // which the softmax has read for the previous tile
+                    if (!(ok = wait_phase(&sm.p_full[t], g & 1, flags, abort_word))) break;
+                    if (!(ok = wait_phase(&sm.v_full[st], (g / kStages) & 1, flags, abort_word))) break;
+                    if (i == 0 && k > 0 && !(ok = wait_phase(&sm.o_free[t], (k - 1) & 1, flags, abort_word)))
+                        break;
+                    tc_fence_after();
+                    const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), kAtomBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(tO, tP + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idO, (i > 0 || kk > 0));
+                    mma_commit(&sm.o_done[t]);
+                    // this tile's last reads of stage st (K(g) by S_t(g), V(g) by the product above)
+                    mma_commit(&sm.kv_empty[st]);
+                }
+            }
+            // every MMA issued above must finish before tensor memory is released
+            mma_commit(&sm.drained[t]);
+            drain_phase(&sm.drained[t], 0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<512>(tmem);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -477,6 +877,29 @@ static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUt
     return cudaGetLastError();
 }
 
+template <int NT>
+static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
+                                    const CUtensorMap& mv, const float* sinks, void* o, float* lse,
+                                    uint32_t* flags, cudaStream_t st) {
+    if (NT == 2) {
+        // the register split above is only safe at exactly this launch value
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_tc_tiles_kernel<NT>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
+    const size_t smem = sizeof(FwdTilesSmem<NT>) + 1024;
+    cudaError_t attr_err = cudaFuncSetAttribute(
+        fwd_tc_tiles_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr_err != cudaSuccess) return attr_err;
+    const int nrb = (P.max_seqlen + kBM - 1) / kBM;
+    dim3 grid((nrb + kWindowTiles - 1) / kWindowTiles, P.h_q / NT, P.nseq);
+    fwd_tc_tiles_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
+                                                               (__nv_bfloat16*)o, lse, flags);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
                    const float* sinks, void* o, float* lse, uint32_t* flags, void*,
                    cudaStream_t st) {
@@ -487,6 +910,10 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
         !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN, P.head_dim))
         return cudaErrorInvalidValue;
     if (P.head_dim == 128) return launch_fwd<1, 128>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    if (P.causal && P.window > 0 && P.window <= 2 * kBN) {
+        if (P.group % 2 == 0) return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, lse, flags, st);
+        return launch_fwd_tiles<1>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    }
     if (P.group % 2 == 0) return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
     return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
 }
