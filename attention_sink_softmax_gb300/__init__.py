@@ -11,7 +11,12 @@ provides device memory and streams.
 
 Tensors: padded q/o/dout [B, N, H_q, d] and k/v [B, N, H_kv, d], or packed
 [T, H, d] with int32 ``cu_seqlens`` [num_seqs + 1] on the device; sinks [H_q]
-fp32; lse [H_q, T] fp32. dtype bf16 or fp32, d = 64.
+fp32; lse [H_q, T] fp32. dtype bf16 or fp32, d = 64 or 128 (decode: 64).
+
+The ``_ex`` forms carry ``o_lo`` (bf16 only): the part of O that its rounding
+to bf16 dropped, written by the forward and used by the backward to form
+D = dO . O from about 16 bits of O instead of the stored 8 (see "Precision of
+D" in include/sink_attn.h). ``sink_attention`` uses them for bf16.
 """
 from __future__ import annotations
 
@@ -27,6 +32,8 @@ from ._abi import SinkAttnError, SinkAttnParams, lib, status_str  # noqa: F401
 __all__ = [
     "SinkAttnParams", "SinkAttnError", "make_params", "sink_attn_workspace_bytes",
     "sink_attn_fwd", "sink_attn_bwd", "sink_attn_bwd_preprocess", "sink_attn_bwd_main",
+    "sink_attn_fwd_ex", "sink_attn_bwd_ex", "sink_attn_bwd_preprocess_ex",
+    "sink_attn_set_wait_limit_ns", "sink_attn_testing_withhold_load",
     "sink_attn_fetch_device_error", "sink_attn_bwd_preprocess_noalloc",
     "sink_attn_noalloc_scratch_bytes", "sink_attn_status_str", "sink_attn_kernel_launches",
     "sink_attn_version", "make_decode_params", "sink_attn_decode_workspace_bytes",
@@ -141,6 +148,68 @@ def sink_attn_fwd(q, k, v, sinks, cu_seqlens=None, *, max_seqlen=None, causal=Tr
     return out, lse
 
 
+def _check_o_lo(o_lo, o):
+    _need_cuda("o_lo", o_lo, o.dtype)
+    if o.dtype != torch.bfloat16:
+        raise ValueError("o_lo is for bf16 outputs only")
+    if o_lo.shape != o.shape or o_lo.device != o.device:
+        raise ValueError("o_lo must have o's shape and device")
+
+
+def sink_attn_fwd_ex(q, k, v, sinks, cu_seqlens=None, *, max_seqlen=None, causal=True, window=0,
+                     softmax_scale=None, out=None, o_lo=None, lse=None, workspace=None,
+                     stream=None, params=None):
+    """Forward that also writes o_lo = bf16(O - bf16(O)) (bf16 only): returns
+    (o, o_lo, lse). See sink_attn_fwd_ex in include/sink_attn.h."""
+    _check_qkv(q, k, v)
+    _need_cuda("sinks", sinks, torch.float32)
+    if q.dtype != torch.bfloat16:
+        raise ValueError("sink_attn_fwd_ex writes o_lo for bf16 inputs only")
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    p = params or make_params(q, k, cu_seqlens, max_seqlen, causal, window, softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if o_lo is None:
+        o_lo = torch.empty_like(q)
+    _check_o_lo(o_lo, out)
+    if lse is None:
+        lse = torch.empty((p.h_q, p.total_tokens), dtype=torch.float32, device=q.device)
+    workspace = _workspace(p, False, q.device, workspace)
+    st = lib().sink_attn_fwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(sinks),
+                                _ptr(cu_seqlens), _ptr(out), _ptr(o_lo), _ptr(lse), _ptr(workspace),
+                                workspace.numel(), _stream(stream, q.device))
+    _abi.check(st, "sink_attn_fwd_ex")
+    return out, o_lo, lse
+
+
+def sink_attn_bwd_ex(q, k, v, sinks, o, o_lo, lse, dout, cu_seqlens=None, *, max_seqlen=None,
+                     causal=True, window=0, softmax_scale=None, dq=None, dk=None, dv=None,
+                     dsinks=None, workspace=None, stream=None, params=None):
+    """Full backward with D formed from o + o_lo: returns (dq, dk, dv, dsinks).
+    See sink_attn_bwd_ex in include/sink_attn.h."""
+    _check_qkv(q, k, v)
+    _need_cuda("o", o, q.dtype)
+    _check_o_lo(o_lo, o)
+    _need_cuda("dout", dout, q.dtype)
+    _need_cuda("lse", lse, torch.float32)
+    _need_cuda("sinks", sinks, torch.float32)
+    if cu_seqlens is not None:
+        _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    p = params or make_params(q, k, cu_seqlens, max_seqlen, causal, window, softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dsinks = torch.empty_like(sinks) if dsinks is None else dsinks
+    workspace = _workspace(p, True, q.device, workspace)
+    st = lib().sink_attn_bwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(sinks),
+                                _ptr(cu_seqlens), _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsinks), _ptr(workspace),
+                                workspace.numel(), _stream(stream, q.device))
+    _abi.check(st, "sink_attn_bwd_ex")
+    return dq, dk, dv, dsinks
+
+
 def sink_attn_bwd(q, k, v, sinks, o, lse, dout, cu_seqlens=None, *, max_seqlen=None,
                   causal=True, window=0, softmax_scale=None, dq=None, dk=None, dv=None,
                   dsinks=None, workspace=None, stream=None, params=None):
@@ -184,6 +253,26 @@ def sink_attn_bwd_preprocess(params, sinks, o, lse, dout, *, delta=None, dsinks=
     return delta, dsinks
 
 
+def sink_attn_bwd_preprocess_ex(params, sinks, o, o_lo, lse, dout, *, delta=None, dsinks=None,
+                                workspace=None, stream=None):
+    """Backward step 1 with delta = dout . (o + o_lo): returns (delta, dsinks)."""
+    _need_cuda("o", o)
+    _check_o_lo(o_lo, o)
+    _need_cuda("dout", dout, o.dtype)
+    _need_cuda("lse", lse, torch.float32)
+    _need_cuda("sinks", sinks, torch.float32)
+    if delta is None:
+        delta = torch.empty((params.h_q, params.total_tokens), dtype=torch.float32, device=o.device)
+    dsinks = torch.empty_like(sinks) if dsinks is None else dsinks
+    workspace = _workspace(params, True, o.device, workspace)
+    st = lib().sink_attn_bwd_preprocess_ex(ctypes.byref(params), _ptr(sinks), _ptr(o), _ptr(o_lo),
+                                           _ptr(lse), _ptr(dout), _ptr(delta), _ptr(dsinks),
+                                           _ptr(workspace), workspace.numel(),
+                                           _stream(stream, o.device))
+    _abi.check(st, "sink_attn_bwd_preprocess_ex")
+    return delta, dsinks
+
+
 def sink_attn_bwd_main(params, q, k, v, lse, delta, dout, cu_seqlens=None, *, dq=None, dk=None,
                        dv=None, workspace=None, stream=None):
     """Backward step 2: returns (dq, dk, dv)."""
@@ -219,9 +308,21 @@ def sink_attn_bwd_preprocess_noalloc(params, sinks, o, lse, dout, *, delta=None,
     if delta is None:
         delta = torch.empty((params.h_q, params.total_tokens), dtype=torch.float32, device=o.device)
     dsinks = torch.empty_like(sinks) if dsinks is None else dsinks
-    st = lib().sink_attn_bwd_preprocess_noalloc(ctypes.byref(params), _ptr(sinks), _ptr(o),
-                                                _ptr(lse), _ptr(dout), _ptr(delta), _ptr(dsinks),
-                                                _stream(stream, o.device))
+    # the kernels write delta [h_q, T] and dsinks [h_q]: a smaller buffer would be overrun
+    _need_cuda("delta", delta, torch.float32)
+    _need_cuda("dsinks", dsinks, torch.float32)
+    if tuple(delta.shape) != (params.h_q, params.total_tokens) or dsinks.numel() != params.h_q:
+        raise ValueError(f"delta must be [{params.h_q}, {params.total_tokens}] and dsinks "
+                         f"[{params.h_q}]")
+    for name, t in (("dout", dout), ("lse", lse), ("sinks", sinks), ("delta", delta),
+                    ("dsinks", dsinks)):
+        if t.device != o.device:
+            raise ValueError(f"{name} is on {t.device}, o on {o.device}")
+    # the library looks up its scratch array on the current device: make it o's
+    with torch.cuda.device(o.device):
+        st = lib().sink_attn_bwd_preprocess_noalloc(ctypes.byref(params), _ptr(sinks), _ptr(o),
+                                                    _ptr(lse), _ptr(dout), _ptr(delta),
+                                                    _ptr(dsinks), _stream(stream, o.device))
     _abi.check(st, "sink_attn_bwd_preprocess_noalloc")
     return delta, dsinks
 
@@ -302,6 +403,19 @@ def sink_attn_status_str(status: int) -> str:
     return status_str(status)
 
 
+def sink_attn_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of every bounded wait inside the kernels, for calls made after this
+    one (process-wide); 0 restores the default of 2 s. Returns the previous limit."""
+    return int(lib().sink_attn_set_wait_limit_ns(int(limit_ns)))
+
+
+def sink_attn_testing_withhold_load(on: bool) -> None:
+    """Test hook (include/sink_attn_testing.h): when on, the 64-wide tensor-core
+    forward and backward stop loading after their first stage, so that their
+    bounded waits run out and the call reports SINK_ERR_TIMEOUT. Tests only."""
+    lib().sink_attn_testing_withhold_load(1 if on else 0)
+
+
 def sink_attn_kernel_launches() -> int:
     """Kernels libsinkattn has enqueued in this process so far."""
     return int(lib().sink_attn_kernel_launches())
@@ -312,23 +426,31 @@ def sink_attn_version() -> int:
 
 
 class SinkAttentionFunction(torch.autograd.Function):
-    """Autograd wrapper: forward and backward both run in libsinkattn."""
+    """Autograd wrapper: forward and backward both run in libsinkattn. With bf16
+    inputs the forward also writes o_lo, which the backward uses to form D."""
 
     @staticmethod
     def forward(ctx, q, k, v, sinks, cu_seqlens, max_seqlen, causal, window, softmax_scale):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         sinks = sinks.contiguous()
         p = make_params(q, k, cu_seqlens, max_seqlen, causal, window, softmax_scale)
-        o, lse = sink_attn_fwd(q, k, v, sinks, cu_seqlens, params=p)
-        ctx.save_for_backward(q, k, v, sinks, o, lse, cu_seqlens)
+        if q.dtype == torch.bfloat16:
+            o, o_lo, lse = sink_attn_fwd_ex(q, k, v, sinks, cu_seqlens, params=p)
+        else:
+            (o, lse), o_lo = sink_attn_fwd(q, k, v, sinks, cu_seqlens, params=p), None
+        ctx.save_for_backward(q, k, v, sinks, o, o_lo, lse, cu_seqlens)
         ctx.params = p
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, sinks, o, lse, cu = ctx.saved_tensors
-        dq, dk, dv, ds = sink_attn_bwd(q, k, v, sinks, o, lse, do.contiguous(), cu,
-                                       params=ctx.params)
+        q, k, v, sinks, o, o_lo, lse, cu = ctx.saved_tensors
+        if o_lo is not None:
+            dq, dk, dv, ds = sink_attn_bwd_ex(q, k, v, sinks, o, o_lo, lse, do.contiguous(), cu,
+                                              params=ctx.params)
+        else:
+            dq, dk, dv, ds = sink_attn_bwd(q, k, v, sinks, o, lse, do.contiguous(), cu,
+                                           params=ctx.params)
         return dq, dk, dv, ds, None, None, None, None, None
 
 

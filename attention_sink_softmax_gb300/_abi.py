@@ -24,12 +24,19 @@ SINK_ERR_SCRATCH_LIMIT = 7
 SINK_BF16 = 0
 SINK_FP32 = 1
 
+SINK_FLAG_TIMEOUT = 1
+SINK_FLAG_SEQ_TOO_LONG = 2
+SINK_FLAG_BAD_SEQLENS = 4
+
 # names declared in include/sink_attn.h, in declaration order
 EXPORTS = (
     "sink_attn_workspace_bytes",
     "sink_attn_fwd",
+    "sink_attn_fwd_ex",
     "sink_attn_bwd",
+    "sink_attn_bwd_ex",
     "sink_attn_bwd_preprocess",
+    "sink_attn_bwd_preprocess_ex",
     "sink_attn_bwd_main",
     "sink_attn_fetch_device_error",
     "sink_attn_bwd_preprocess_noalloc",
@@ -37,9 +44,12 @@ EXPORTS = (
     "sink_attn_decode_workspace_bytes",
     "sink_attn_decode",
     "sink_attn_status_str",
+    "sink_attn_set_wait_limit_ns",
     "sink_attn_kernel_launches",
     "sink_attn_version",
 )
+# declared in include/sink_attn_testing.h
+TESTING_EXPORTS = ("sink_attn_testing_withhold_load",)
 
 
 class SinkAttnParams(ctypes.Structure):
@@ -93,10 +103,16 @@ def lib():
             L.sink_attn_workspace_bytes.restype = ctypes.c_size_t
             L.sink_attn_fwd.argtypes = [_PP] + [_P] * 7 + [_P, ctypes.c_size_t, _P]
             L.sink_attn_fwd.restype = ctypes.c_int
+            L.sink_attn_fwd_ex.argtypes = [_PP] + [_P] * 8 + [_P, ctypes.c_size_t, _P]
+            L.sink_attn_fwd_ex.restype = ctypes.c_int
             L.sink_attn_bwd.argtypes = [_PP] + [_P] * 12 + [_P, ctypes.c_size_t, _P]
             L.sink_attn_bwd.restype = ctypes.c_int
+            L.sink_attn_bwd_ex.argtypes = [_PP] + [_P] * 13 + [_P, ctypes.c_size_t, _P]
+            L.sink_attn_bwd_ex.restype = ctypes.c_int
             L.sink_attn_bwd_preprocess.argtypes = [_PP] + [_P] * 6 + [_P, ctypes.c_size_t, _P]
             L.sink_attn_bwd_preprocess.restype = ctypes.c_int
+            L.sink_attn_bwd_preprocess_ex.argtypes = [_PP] + [_P] * 7 + [_P, ctypes.c_size_t, _P]
+            L.sink_attn_bwd_preprocess_ex.restype = ctypes.c_int
             L.sink_attn_bwd_main.argtypes = [_PP] + [_P] * 10 + [_P, ctypes.c_size_t, _P]
             L.sink_attn_bwd_main.restype = ctypes.c_int
             L.sink_attn_fetch_device_error.argtypes = [_P, ctypes.c_size_t, _P,
@@ -112,6 +128,10 @@ def lib():
             L.sink_attn_decode.restype = ctypes.c_int
             L.sink_attn_status_str.argtypes = [ctypes.c_int]
             L.sink_attn_status_str.restype = ctypes.c_char_p
+            L.sink_attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.sink_attn_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.sink_attn_testing_withhold_load.argtypes = [ctypes.c_int]
+            L.sink_attn_testing_withhold_load.restype = None
             L.sink_attn_kernel_launches.argtypes = []
             L.sink_attn_kernel_launches.restype = ctypes.c_uint64
             L.sink_attn_version.argtypes = []

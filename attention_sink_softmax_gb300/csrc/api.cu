@@ -13,12 +13,21 @@
 #include <atomic>
 
 #include "../../include/sink_attn.h"
+#include "../../include/sink_attn_testing.h"
 #include "kernels.h"
 #include "tc.h"
+#include "validate.h"
 
 using namespace sinkattn;
 
+static_assert(kFlagTimeout == SINK_FLAG_TIMEOUT && kFlagSeqTooLong == SINK_FLAG_SEQ_TOO_LONG &&
+                  kFlagBadSeqlens == SINK_FLAG_BAD_SEQLENS,
+              "device flag bits as published in sink_attn.h");
+
 static std::atomic<uint64_t> g_launches{0};
+// limit of every bounded device wait, and the test hook that withholds loads
+static std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+static std::atomic<int> g_withhold_load{0};
 
 namespace sinkattn {
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -45,7 +54,10 @@ bool device_accessible(const void* x) {
 }
 
 
-sink_status_t validate(const sink_attn_params_t* p) {
+}  // namespace
+
+namespace sinkattn {
+sink_status_t validate_params(const sink_attn_params_t* p) {
     if (!p) return SINK_ERR_INVALID_ARG;
     if (p->batch < 0 || p->max_seqlen < 0 || p->total_tokens < 0) return SINK_ERR_INVALID_ARG;
     if (p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv != 0) return SINK_ERR_INVALID_ARG;
@@ -60,6 +72,12 @@ sink_status_t validate(const sink_attn_params_t* p) {
     if (p->head_dim != 64 && p->head_dim != 128) return SINK_ERR_UNSUPPORTED;
     return SINK_OK;
 }
+
+}  // namespace sinkattn
+
+namespace {
+
+sink_status_t validate(const sink_attn_params_t* p) { return validate_params(p); }
 
 // Padded layout: total_tokens must equal batch * max_seqlen.
 sink_status_t validate_layout(const sink_attn_params_t* p, const int32_t* cu) {
@@ -82,6 +100,8 @@ Problem make_problem(const sink_attn_params_t* p, const int32_t* cu) {
     P.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     P.scale_log2 = P.scale * kLog2e;
     P.cu = cu;
+    P.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    P.withhold_load = g_withhold_load.load(std::memory_order_relaxed);
     return P;
 }
 
@@ -124,16 +144,25 @@ size_t sink_attn_workspace_bytes(const sink_attn_params_t* params, int is_bwd) {
     return is_bwd ? bwd_layout(params).total : fwd_bytes(params);
 }
 
-sink_status_t sink_attn_fwd(const sink_attn_params_t* params, const void* q, const void* k,
-                            const void* v, const float* sinks, const int32_t* cu_seqlens, void* o,
-                            float* lse, void* workspace, size_t workspace_bytes,
-                            sink_stream_t stream) {
+// o_lo: NULL, or bf16 [T, h_q, d] (bf16 params only)
+static sink_status_t check_o_lo(const sink_attn_params_t* p, const void* o_lo) {
+    if (!o_lo) return SINK_OK;
+    if (p->dtype != SINK_BF16) return SINK_ERR_INVALID_ARG;
+    if (!empty(p) && !all_aligned({o_lo})) return SINK_ERR_INVALID_ARG;
+    return SINK_OK;
+}
+
+sink_status_t sink_attn_fwd_ex(const sink_attn_params_t* params, const void* q, const void* k,
+                               const void* v, const float* sinks, const int32_t* cu_seqlens,
+                               void* o, void* o_lo, float* lse, void* workspace,
+                               size_t workspace_bytes, sink_stream_t stream) {
     sink_status_t st = validate(params);
     if (st != SINK_OK) return st;
     if ((st = validate_layout(params, cu_seqlens)) != SINK_OK) return st;
     if (!workspace || !aligned16(workspace) || !device_accessible(workspace)) return SINK_ERR_WORKSPACE;
     if (workspace_bytes < fwd_bytes(params)) return SINK_ERR_WORKSPACE;
     if (!empty(params) && !all_aligned({q, k, v, sinks, o, lse})) return SINK_ERR_INVALID_ARG;
+    if ((st = check_o_lo(params, o_lo)) != SINK_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t* flags = (uint32_t*)workspace;
     cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t), s);
@@ -141,16 +170,25 @@ sink_status_t sink_attn_fwd(const sink_attn_params_t* params, const void* q, con
     const Problem P = make_problem(params, cu_seqlens);
     const bool bf16 = params->dtype == SINK_BF16;
     if (tc_fwd_supported(P, bf16))
-        e = tc_fwd(P, q, k, v, sinks, o, lse, flags, (char*)workspace + kHeaderBytes, s);
+        e = tc_fwd(P, q, k, v, sinks, o, o_lo, lse, flags, (char*)workspace + kHeaderBytes, s);
     else
-        e = simt_fwd(P, bf16, q, k, v, sinks, o, lse, flags, s);
+        e = simt_fwd(P, bf16, q, k, v, sinks, o, o_lo, lse, flags, s);
     return cuda_status(e);
 }
 
-sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params, const float* sinks,
-                                       const void* o, const float* lse, const void* dout,
-                                       float* delta, float* dsinks, void* workspace,
-                                       size_t workspace_bytes, sink_stream_t stream) {
+sink_status_t sink_attn_fwd(const sink_attn_params_t* params, const void* q, const void* k,
+                            const void* v, const float* sinks, const int32_t* cu_seqlens, void* o,
+                            float* lse, void* workspace, size_t workspace_bytes,
+                            sink_stream_t stream) {
+    return sink_attn_fwd_ex(params, q, k, v, sinks, cu_seqlens, o, nullptr, lse, workspace,
+                            workspace_bytes, stream);
+}
+
+sink_status_t sink_attn_bwd_preprocess_ex(const sink_attn_params_t* params, const float* sinks,
+                                          const void* o, const void* o_lo, const float* lse,
+                                          const void* dout, float* delta, float* dsinks,
+                                          void* workspace, size_t workspace_bytes,
+                                          sink_stream_t stream) {
     sink_status_t st = validate(params);
     if (st != SINK_OK) return st;
     if (!workspace || !aligned16(workspace) || !device_accessible(workspace)) return SINK_ERR_WORKSPACE;
@@ -158,13 +196,24 @@ sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params, const f
     if (workspace_bytes < L.total) return SINK_ERR_WORKSPACE;
     if (!all_aligned({sinks, dsinks})) return SINK_ERR_INVALID_ARG;
     if (params->total_tokens > 0 && !all_aligned({o, lse, dout, delta})) return SINK_ERR_INVALID_ARG;
+    if (o_lo && (params->dtype != SINK_BF16 ||
+                 (params->total_tokens > 0 && !all_aligned({o_lo}))))
+        return SINK_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return SINK_ERR_CUDA;
     const Problem P = make_problem(params, nullptr);
-    e = bwd_preprocess(P, params->dtype == SINK_BF16, sinks, o, lse, dout, delta, dsinks,
+    e = bwd_preprocess(P, params->dtype == SINK_BF16, sinks, o, o_lo, lse, dout, delta, dsinks,
                        (float*)((char*)workspace + L.partial), s);
     return cuda_status(e);
+}
+
+sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params, const float* sinks,
+                                       const void* o, const float* lse, const void* dout,
+                                       float* delta, float* dsinks, void* workspace,
+                                       size_t workspace_bytes, sink_stream_t stream) {
+    return sink_attn_bwd_preprocess_ex(params, sinks, o, nullptr, lse, dout, delta, dsinks,
+                                       workspace, workspace_bytes, stream);
 }
 
 sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params, const void* q, const void* k,
@@ -191,15 +240,15 @@ sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params, const void* q
     else if (tc_bwd128_supported(P, bf16))
         e = tc_bwd128(P, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace, s);
     else
-        e = simt_bwd_main(P, bf16, q, k, v, lse, delta, dout, dq, dk, dv, s);
+        e = simt_bwd_main(P, bf16, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace, s);
     return cuda_status(e);
 }
 
-sink_status_t sink_attn_bwd(const sink_attn_params_t* params, const void* q, const void* k,
-                            const void* v, const float* sinks, const int32_t* cu_seqlens,
-                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                            void* dv, float* dsinks, void* workspace, size_t workspace_bytes,
-                            sink_stream_t stream) {
+sink_status_t sink_attn_bwd_ex(const sink_attn_params_t* params, const void* q, const void* k,
+                               const void* v, const float* sinks, const int32_t* cu_seqlens,
+                               const void* o, const void* o_lo, const float* lse, const void* dout,
+                               void* dq, void* dk, void* dv, float* dsinks, void* workspace,
+                               size_t workspace_bytes, sink_stream_t stream) {
     sink_status_t st = validate(params);
     if (st != SINK_OK) return st;
     if ((st = validate_layout(params, cu_seqlens)) != SINK_OK) return st;
@@ -209,12 +258,22 @@ sink_status_t sink_attn_bwd(const sink_attn_params_t* params, const void* q, con
     if (!all_aligned({sinks, dsinks})) return SINK_ERR_INVALID_ARG;
     if (!empty(params) && !all_aligned({q, k, v, o, lse, dout, dq, dk, dv}))
         return SINK_ERR_INVALID_ARG;
+    if ((st = check_o_lo(params, o_lo)) != SINK_OK) return st;
     float* delta = (float*)((char*)workspace + L.delta);
-    st = sink_attn_bwd_preprocess(params, sinks, o, lse, dout, delta, dsinks, workspace,
-                                  workspace_bytes, stream);
+    st = sink_attn_bwd_preprocess_ex(params, sinks, o, o_lo, lse, dout, delta, dsinks, workspace,
+                                     workspace_bytes, stream);
     if (st != SINK_OK) return st;
     return sink_attn_bwd_main(params, q, k, v, cu_seqlens, lse, delta, dout, dq, dk, dv, workspace,
                               workspace_bytes, stream);
+}
+
+sink_status_t sink_attn_bwd(const sink_attn_params_t* params, const void* q, const void* k,
+                            const void* v, const float* sinks, const int32_t* cu_seqlens,
+                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                            void* dv, float* dsinks, void* workspace, size_t workspace_bytes,
+                            sink_stream_t stream) {
+    return sink_attn_bwd_ex(params, q, k, v, sinks, cu_seqlens, o, nullptr, lse, dout, dq, dk, dv,
+                            dsinks, workspace, workspace_bytes, stream);
 }
 
 sink_status_t sink_attn_fetch_device_error(void* workspace, size_t workspace_bytes,
@@ -247,6 +306,7 @@ DecodeArgs decode_args(const sink_attn_params_t* p) {
     a.nsplit = decode_splits(p->batch, p->h_kv, p->max_seqlen);
     const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * kLog2e;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     return a;
 }
 
@@ -315,6 +375,14 @@ const char* sink_attn_status_str(sink_status_t status) {
 
 uint64_t sink_attn_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int sink_attn_version(void) { return 100; }
+uint64_t sink_attn_set_wait_limit_ns(uint64_t limit_ns) {
+    return g_wait_ns.exchange(limit_ns ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+}
+
+void sink_attn_testing_withhold_load(int on) {
+    g_withhold_load.store(on ? 1 : 0, std::memory_order_relaxed);
+}
+
+int sink_attn_version(void) { return 200; }
 
 }  // extern "C"

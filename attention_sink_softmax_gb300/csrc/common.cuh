@@ -18,6 +18,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Device flag bits written into the first word of the workspace.
 constexpr uint32_t kFlagTimeout = 1u << 0;    // a bounded wait gave up
 constexpr uint32_t kFlagSeqTooLong = 1u << 1;  // a sequence longer than max_seqlen
+constexpr uint32_t kFlagBadSeqlens = 1u << 2;  // cu_seqlens is not a non-decreasing run from 0 within T
+
+// Limit of every bounded wait in the tensor-core kernels.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
 struct Problem {
     int nseq;          // number of sequences
@@ -29,6 +33,8 @@ struct Problem {
     float scale;       // softmax scale on Q.K
     float scale_log2;  // scale * log2(e): scores in base-2 units
     const int32_t* cu; // device cu_seqlens or nullptr (padded: sequence s = [s*N, s*N+N))
+    uint64_t wait_ns;  // limit of each bounded wait (kDefaultWaitNs unless a test lowers it)
+    int withhold_load; // test hook: the forward / backward producer stops after its first stage
 };
 
 // Decode (one query per entry against a key/value cache), see decode.cu.
@@ -41,16 +47,31 @@ struct DecodeArgs {
     int window;       // <= 0: whole context; W: its last W keys
     int nsplit;       // chunks of each query's keys
     float scale_log2;
+    uint64_t wait_ns; // limit of each bounded wait
 };
 
-__device__ __forceinline__ void seq_bounds(const Problem& P, int s, int& start, int& len) {
-    if (P.cu) {
-        start = __ldg(P.cu + s);
-        len = __ldg(P.cu + s + 1) - start;
-    } else {
+// Bounds of sequence s, checked: with packed sequences, cu_seqlens comes from
+// device memory that the host never reads, so a CTA verifies
+// 0 <= cu[s] <= cu[s+1] <= total (and cu[0] == 0 for s = 0) before it touches
+// any row. A CTA whose sequence fails returns false and raises
+// kFlagBadSeqlens; it must then return before any load, store or barrier.
+__device__ __forceinline__ bool seq_bounds_checked(const Problem& P, int s, int& start, int& len,
+                                                   uint32_t* flags) {
+    if (!P.cu) {
         start = s * P.max_seqlen;
         len = P.max_seqlen;
+        return true;
     }
+    const int a = __ldg(P.cu + s), b = __ldg(P.cu + s + 1);
+    if (a < 0 || b < a || b > P.total || (s == 0 && a != 0)) {
+        if (threadIdx.x == 0) atomicOr(flags, kFlagBadSeqlens);
+        start = 0;
+        len = 0;
+        return false;
+    }
+    start = a;
+    len = b - a;
+    return true;
 }
 
 // First allowed key of row i.

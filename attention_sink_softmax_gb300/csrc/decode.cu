@@ -415,7 +415,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     int done = 0;  // own stages consumed
     for (; done < mine; ++done) {
         const int slot = done % kSlots;
-        if (!tc::wait_phase(&wfull[slot], (done / kSlots) & 1, flags, abort_word)) break;
+        if (!tc::wait_phase(&wfull[slot], (done / kSlots) & 1, flags, abort_word, a.wait_ns)) break;
         const int nk = min(kKeys, k_end - (k_begin + (warp + done * kWarps) * kKeys));
         uint8_t* kbox = wslots + slot * kStageBytes;
         const uint32_t kb = tc::smem_u32(kbox), vb = kb + kBoxBytes;
@@ -512,7 +512,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     }
     // after a timeout: let the copies still in flight land before the CTA leaves
     if (done < mine && lane == 0)
-        for (int j = done; j < min(mine, done + kSlots); ++j) tc::drain_phase(&wfull[j % kSlots], (j / kSlots) & 1);
+        for (int j = done; j < min(mine, done + kSlots); ++j) tc::drain_phase(&wfull[j % kSlots], (j / kSlots) & 1, a.wait_ns);
 
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)

@@ -11,19 +11,27 @@ namespace sinkattn {
 // Counts every kernel launch the library enqueues (sink_attn_kernel_launches).
 void count_launches(unsigned n);
 
+// f16 copy of `elems` bf16 values (a multiple of 8; 16-byte aligned buffers),
+// exact within f16's range (convert.cu).
+cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st);
+
 // CUDA-core path (any dtype the ABI accepts, head_dim 64).
+// o_lo (nullable, bf16 only): receives bf16(O - bf16(O)) per element.
 cudaError_t simt_fwd(const Problem& P, bool bf16, const void* q, const void* k, const void* v,
-                     const float* sinks, void* o, float* lse, uint32_t* flags, cudaStream_t st);
+                     const float* sinks, void* o, void* o_lo, float* lse, uint32_t* flags,
+                     cudaStream_t st);
 cudaError_t simt_bwd_main(const Problem& P, bool bf16, const void* q, const void* k, const void* v,
                           const float* lse, const float* delta, const void* dout, void* dq,
-                          void* dk, void* dv, cudaStream_t st);
+                          void* dk, void* dv, uint32_t* flags, cudaStream_t st);
 
 // Backward step 1 (memory-bound): delta [h_q, T] and dsinks [h_q] via
 // per-chunk partials [h_q, preprocess_chunks(T)] reduced in a fixed order.
 int preprocess_chunks(int total);
+// o_lo (nullable, bf16 only): the low-order part of O written by the forward;
+// when given, delta = dout . (o + o_lo).
 cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, const void* o,
-                           const float* lse, const void* dout, float* delta, float* dsinks,
-                           float* partial, cudaStream_t st);
+                           const void* o_lo, const float* lse, const void* dout, float* delta,
+                           float* dsinks, float* partial, cudaStream_t st);
 
 // Decode (decode.cu): split kernel (+ merge kernel on the CUDA-core path).
 // `part` holds decode_partial_floats(batch, h_q) floats; `counters` holds

@@ -27,6 +27,7 @@
 
 #include "../../include/sink_attn.h"
 #include "kernels.h"
+#include "validate.h"
 
 namespace {
 
@@ -77,10 +78,9 @@ sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t* p, cons
                                                float* delta, float* dsinks,
                                                sink_stream_t stream) {
     using namespace sinkattn;
-    if (!p || p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv || p->total_tokens < 0)
-        return SINK_ERR_INVALID_ARG;
-    if (p->dtype != SINK_BF16 && p->dtype != SINK_FP32) return SINK_ERR_INVALID_ARG;
-    if (p->head_dim != 64 && p->head_dim != 128) return SINK_ERR_UNSUPPORTED;
+    // the same field checks (and status codes) as sink_attn_bwd_preprocess
+    const sink_status_t st = validate_params(p);
+    if (st != SINK_OK) return st;
     const size_t need = (size_t)p->h_q * (size_t)preprocess_chunks(p->total_tokens);
     if (need > kNoallocScratchFloats) return SINK_ERR_SCRATCH_LIMIT;
     if (!ok_ptr(sinks) || !ok_ptr(dsinks)) return SINK_ERR_INVALID_ARG;
@@ -96,8 +96,9 @@ sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t* p, cons
     P.h_kv = p->h_kv;
     P.group = p->h_q / p->h_kv;
     P.head_dim = p->head_dim;
-    cudaError_t e = bwd_preprocess(P, p->dtype == SINK_BF16, sinks, o, lse, dout, delta, dsinks,
-                                   scratch, (cudaStream_t)stream);
+    P.wait_ns = kDefaultWaitNs;
+    cudaError_t e = bwd_preprocess(P, p->dtype == SINK_BF16, sinks, o, nullptr, lse, dout, delta,
+                                   dsinks, scratch, (cudaStream_t)stream);
     return e == cudaSuccess ? SINK_OK : SINK_ERR_CUDA;
 }
 

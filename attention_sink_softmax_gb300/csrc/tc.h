@@ -11,8 +11,8 @@ namespace sinkattn {
 bool tc_fwd_supported(const Problem& P, bool bf16);
 size_t tc_fwd_workspace_bytes(const Problem& P, bool bf16);
 cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
-                   const float* sinks, void* o, float* lse, uint32_t* flags, void* workspace,
-                   cudaStream_t st);
+                   const float* sinks, void* o, void* o_lo, float* lse, uint32_t* flags,
+                   void* workspace, cudaStream_t st);
 
 bool tc_bwd_supported(const Problem& P, bool bf16);
 size_t tc_bwd_workspace_bytes(const Problem& P, bool bf16);

@@ -23,6 +23,11 @@
 //   dV  += P^T dO    A = P^T  (tensor memory, from registers) B = dO
 //   dK  += dS^T Q    A = dS^T (tensor memory, from registers) B = Q
 //   dQ   = dS K      A = dS   (smem: needs query rows as M)   B = K  (smem)
+// dS feeds dQ and dK in f16 (with large logits bf16's 8 bits of dS push dQ and
+// dK out of tolerance), so their B operands K and Q are f16 too: tc_bwd first
+// writes f16 copies of Q and K into the workspace (convert.cu), the tiles are
+// loaded from them, and S^T = K Q^T runs in f16 as well. dP^T and dV stay
+// bf16. bf16 -> f16 is exact for magnitudes within f16's range.
 // S^T and dP^T share one 128-column region: the elementwise warps read S^T
 // into registers, then dP^T is computed into the same columns while they
 // exponentiate. Two threads issue MMAs: one issues S^T and dP^T, the other
@@ -99,7 +104,7 @@ __device__ __forceinline__ uint2 split3_bf16(float v) {
 }
 
 struct BwdSmem {
-    alignas(1024) __nv_bfloat16 k[kBN * kD];  // B operand of dQ
+    alignas(1024) __nv_bfloat16 k[kBN * kD];  // B operand of dQ (converted to f16 in place)
     alignas(1024) __nv_bfloat16 q[kQStages][kBM * kD];
     alignas(1024) __nv_bfloat16 dout[kQStages][kBM * kD];
     // dS, double-buffered by step parity: two 16 KB atoms (query rows 0..63 and
@@ -157,7 +162,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int hk = blockIdx.y;
     const int seq = blockIdx.z;
     int start, L;
-    seq_bounds(P, seq, start, L);
+    if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     const int k0 = kb * kBN;
     if (k0 >= L) return;  // uniform for the CTA, before any barrier or TMEM use
 
@@ -211,8 +216,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float sc = P.scale_log2;
         {
-            // A operands of S^T and dP^T: warpgroup 0 places this key's K row,
-            // warpgroup 1 its V row (zeros past the sequence)
+            // A operands of S^T and dP^T: warpgroup 0 places this key's K row (f16,
+            // from the f16 copy), warpgroup 1 its V row (bf16); zeros past the sequence
             uint32_t row[32];
             const __nv_bfloat16* src = (w == 0 ? kg : vg) + ((size_t)(start + kp) * P.h_kv + hk) * kD;
 #pragma unroll
@@ -239,7 +244,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bool s_ready = false;  // S^T of this step seen complete by an early poll
         for (int it = 0; it < nsteps; ++it) {
             const int q0 = (qb_lo + it % nq) * kBM;
-            ok = __all_sync(0xffffffffu, s_ready || wait_phase(&sm.s_full, it & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, s_ready || wait_phase(&sm.s_full, it & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float p[64];  // P^T for this key and query rows [64w, 64w+64)
@@ -279,10 +284,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     p[j] = allowed ? p[j] : 0.f;
                 }
             }
-            uint32_t pp[32], pd[32];  // packed bf16 pairs of P^T and dS^T
+            // packed pairs: P^T in bf16 (tensor memory, A of dV), dS^T in f16 (tensor
+            // memory, A of dK, and shared memory, A of dQ; their B operands Q and K
+            // are f16 too): f16's 11 bits keep dQ and dK within tolerance when logits
+            // are large
+            uint32_t pp[32], pd[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) pp[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, it & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, it & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             {
@@ -294,41 +303,38 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const bool pd_ready = it == 0 || mbar_test_wait(&sm.pd_free, (it - 1) & 1);
                 const bool ds_ready = it <= 1 || mbar_test_wait(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1);
                 tmem_ld_wait();
+                if (it > 1) {
+                    ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
+                                                                        ((it >> 1) - 1) & 1, flags,
+                                                                        abort_word, P.wait_ns));
+                    if (!ok) break;
+                }
+                // dS row of this key (f16): 64 query rows = 128 bytes of atom w of the
+                // step's buffer; written before the tensor-memory stores below so that
+                // the proxy fence after them finds these stores done
+                uint8_t* atom = sm.ds[it & 1][w];
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) {
+                for (int c16 = 0; c16 < 8; ++c16) {
                     // dS = P (dP - delta), two columns per paired op (the MMA subtracted delta)
-                    const uint32_t* d = dv64 + j;
-                    const uint64_t t01 = f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1]));
-                    const uint64_t t23 = f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3]));
-                    float y0, y1, y2, y3;
-                    f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t01), y0, y1);
-                    f2_unpack(f2_mul(f2_pack(p[j + 2], p[j + 3]), t23), y2, y3);
-                    pd[j / 2] = pack_bf16x2(y0, y1);
-                    pd[j / 2 + 1] = pack_bf16x2(y2, y3);
+                    float y[8];
+#pragma unroll
+                    for (int u = 0; u < 8; u += 2) {
+                        const int j = 8 * c16 + u;
+                        const uint64_t t = f2_pack(__uint_as_float(dv64[j]), __uint_as_float(dv64[j + 1]));
+                        f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t), y[u], y[u + 1]);
+                        pd[j / 2] = pack_f16x2(y[u], y[u + 1]);
+                    }
+                    *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) =
+                        make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
                 }
                 // dP^T has been read: the next step's S^T may overwrite the columns
                 tc_fence_before();
                 mbar_arrive(&sm.dp_loaded);
                 if (it > 0) {
                     ok = __all_sync(0xffffffffu, pd_ready || wait_phase(&sm.pd_free, (it - 1) & 1, flags,
-                                                                        abort_word));
+                                                                        abort_word, P.wait_ns));
                     if (!ok) break;
                 }
-                if (it > 1) {
-                    ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
-                                                                        ((it >> 1) - 1) & 1, flags,
-                                                                        abort_word));
-                    if (!ok) break;
-                }
-            }
-            // dS row of this key: 64 query rows = 128 bytes of atom w (A operand of dQ);
-            // written before the tensor-memory stores so that the proxy fence below
-            // finds them done
-            uint8_t* atom = sm.ds[it & 1][w];
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
-                const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
-                *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
@@ -343,7 +349,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled). These
         // warps do not wait on every phase of grads_done, so a parity wait on it
         // could match a phase two steps back: the single-phase acc_done is used.
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.acc_done, 0, flags, abort_word));
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.acc_done, 0, flags, abort_word, P.wait_ns));
         if (ok) {
             tc_fence_after();
             uint32_t a[32], b[32];
@@ -372,7 +378,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int h = hk * P.group + it / nq;
             const int q0 = (qb_lo + it % nq) * kBM;
             // one decision for all four drain warps (they meet at named barriers below)
-            if (!vote_all_128(1, wait_phase(&sm.grads_done, it & 1, flags, abort_word))) break;
+            if (!vote_all_128(1, wait_phase(&sm.grads_done, it & 1, flags, abort_word, P.wait_ns))) break;
             tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -425,9 +431,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int st = it % kQStages;
                 const int h = hk * P.group + it / nq;
                 const int q0 = (qb_lo + it % nq) * kBM;
+                // test hook (off unless a test sets it): no load after the first step,
+                // so the consumers' bounded waits run out
+                if (P.withhold_load && it == 1) break;
                 if (it >= kQStages &&
                     !__all_sync(0xffffffffu, wait_phase(&sm.q_empty[st], ((it / kQStages) - 1) & 1,
-                                                        flags, abort_word)))
+                                                        flags, abort_word, P.wait_ns)))
                     break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&sm.q_full[st], 2 * kTileBytes);
@@ -454,22 +463,23 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 issued = it + 1;
             }
             if (lane == 0) {
-                drain_phase(&sm.k_full, 0);
+                drain_phase(&sm.k_full, 0, P.wait_ns);
                 for (int it = max(0, issued - kQStages); it < issued; ++it)
-                    drain_phase(&sm.q_full[it % kQStages], (it / kQStages) & 1);
+                    drain_phase(&sm.q_full[it % kQStages], (it / kQStages) & 1, P.wait_ns);
             }
         } else if (warp == 9 && lane == 0) {
             // -------------------------------------------------------- MMA issuer 1: S^T, dP^T
-            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // A tmem, B K-major
+            constexpr uint32_t idSS = idesc_bf16(kBN, kBM, 0, 0);  // A tmem, B K-major: bf16
+            constexpr uint32_t idS16 = idesc_f16(kBN, kBM, 0, 0);  // the same in f16 (K, Q)
             const uint64_t dones = smem_desc_noswizzle(smem_u32(sm.aug_ones), kAugLBO, kAugSBO);
-            bool ok = wait_phase(&sm.kv_tmem, 0, flags, abort_word) &&
-                      wait_phase(&sm.q_full[0], 0, flags, abort_word);
+            bool ok = wait_phase(&sm.kv_tmem, 0, flags, abort_word, P.wait_ns) &&
+                      wait_phase(&sm.q_full[0], 0, flags, abort_word, P.wait_ns);
             auto issue_s = [&](int st) {  // S^T - LSE / scale = K Q^T + ones (-LSE / scale)^T
                 tc_fence_after();
                 const uint64_t dq_ = smem_desc_sw128(smem_u32(sm.q[st]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    mma_ts(tmem + kColSdP, tmem + kColK + kk * 8, dq_ + 2 * kk, idSS, kk > 0);
+                    mma_ts(tmem + kColSdP, tmem + kColK + kk * 8, dq_ + 2 * kk, idS16, kk > 0);
                 mma_ss(tmem + kColSdP, dones, smem_desc_noswizzle(smem_u32(sm.aug_lse[st]), kAugLBO, kAugSBO),
                        idSS, 1);
                 mma_commit(&sm.s_full);
@@ -480,7 +490,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int st1 = (it + 1) % kQStages;
                 // early poll of the next step's Q / dO stage (answer used after dP)
                 const bool q_ready = it + 1 >= nsteps || mbar_test_wait(&sm.q_full[st1], ((it + 1) / kQStages) & 1);
-                if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.s_loaded, it & 1, flags, abort_word, P.wait_ns))) break;
                 // dP^T - delta = V dO^T + ones (-delta)^T, into the columns S^T was read from
                 tc_fence_after();
                 const uint64_t ddo = smem_desc_sw128(smem_u32(sm.dout[st]), 16, 1024);
@@ -493,25 +503,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mma_commit(&sm.q_empty[st]);  // this issuer's last read of the step's Q / dO stage
                 if (it + 1 < nsteps) {
                     if (!(ok = q_ready || wait_phase(&sm.q_full[st1], ((it + 1) / kQStages) & 1, flags,
-                                                     abort_word)))
+                                                     abort_word, P.wait_ns)))
                         break;
-                    if (!(ok = wait_phase(&sm.dp_loaded, it & 1, flags, abort_word))) break;
+                    if (!(ok = wait_phase(&sm.dp_loaded, it & 1, flags, abort_word, P.wait_ns))) break;
                     issue_s(st1);
                 }
             }
             // every MMA issued above must finish before tensor memory is released
             mma_commit(&sm.drained[0]);
-            drain_phase(&sm.drained[0], 0);
+            drain_phase(&sm.drained[0], 0, P.wait_ns);
         } else if (warp == 10 && lane == 0) {
             // -------------------------------------------------------- MMA issuer 2: dV, dK, dQ
-            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);  // dV, dK: A tmem, B MN-major
-            constexpr uint32_t idQ = idesc_bf16(kBM, kD, 1, 1);  // dQ: A and B MN-major (smem)
+            constexpr uint32_t idG = idesc_bf16(kBN, kD, 0, 1);    // dV: A tmem, B MN-major, bf16
+            constexpr uint32_t idG16 = idesc_f16(kBN, kD, 0, 1);   // dK: the same in f16
+            constexpr uint32_t idQ = idesc_f16(kBM, kD, 1, 1);  // dQ: f16, A and B MN-major (smem)
             const uint64_t dKmn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
-            bool ok = wait_phase(&sm.k_full, 0, flags, abort_word);
+            bool ok = wait_phase(&sm.k_full, 0, flags, abort_word, P.wait_ns);
             for (int j = 0; ok && j < nsteps; ++j) {
                 const int st = j % kQStages;
                 // dV += P^T dO, dK += dS^T Q  (K = query rows)
-                if (!(ok = wait_phase(&sm.ds_full, j & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.ds_full, j & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 const uint64_t ddo_mn = smem_desc_sw128(smem_u32(sm.dout[st]), 1024, 1024);
                 const uint64_t dq_mn = smem_desc_sw128(smem_u32(sm.q[st]), 1024, 1024);
@@ -519,14 +530,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 for (int kk = 0; kk < kBM / 16; ++kk) {
                     const uint64_t boff = (uint64_t)((kk * 2048) >> 4);
                     mma_ts(tmem + kColDV, tmem + kColP + kk * 8, ddo_mn + boff, idG, j > 0 || kk > 0);
-                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG, j > 0 || kk > 0);
+                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, dq_mn + boff, idG16, j > 0 || kk > 0);
                 }
                 // P^T, dS^T and the step's Q / dO stage are no longer read
                 mma_commit(&sm.pd_free);
                 mma_commit(&sm.q_empty[st]);
                 // dQ = dS K  (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
                 if (j > 0) {
-                    if (!(ok = wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word))) break;
+                    if (!(ok = wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word, P.wait_ns))) break;
                     tc_fence_after();
                 }
 #pragma unroll
@@ -539,7 +550,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (ok) mma_commit(&sm.acc_done);
             mma_commit(&sm.drained[1]);
-            drain_phase(&sm.drained[1], 0);
+            drain_phase(&sm.drained[1], 0, P.wait_ns);
         }
     }
     tc_fence_before();
@@ -566,9 +577,14 @@ bool tc_bwd_supported(const Problem& P, bool bf16) {
     return bf16 && P.head_dim == kD && P.total > 0;
 }
 
+// [dQ accumulator fp32 [T, h_q, 64]][Q in f16 [T, h_q, 64]][K in f16 [T, h_kv, 64]]
+static size_t acc_bytes(const Problem& P) { return sizeof(float) * (size_t)P.total * P.h_q * kD; }
+static size_t q16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_q * kD; }
+static size_t k16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_kv * kD; }
+
 size_t tc_bwd_workspace_bytes(const Problem& P, bool bf16) {
     if (!bf16 || P.head_dim != kD) return 0;
-    return sizeof(float) * (size_t)P.total * P.h_q * kD;  // dQ accumulator
+    return acc_bytes(P) + q16_bytes(P) + k16_bytes(P);
 }
 
 cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v,
@@ -576,15 +592,21 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
                    void* dv, uint32_t* flags, void* workspace, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
     float* acc = static_cast<float*>(workspace);
+    // f16 copies of Q and K for the f16 products (the same 2-byte layout)
+    void* q16 = static_cast<char*>(workspace) + acc_bytes(P);
+    void* k16 = static_cast<char*>(q16) + q16_bytes(P);
+    cudaError_t e = convert_bf16_to_f16(q, q16, (size_t)P.total * P.h_q * kD, st);
+    if (e == cudaSuccess) e = convert_bf16_to_f16(k, k16, (size_t)P.total * P.h_kv * kD, st);
+    if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mdo, mdq;
-    if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM) ||
-        !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN) ||
+    if (!make_head_tile_map(&mq, q16, P.total, P.h_q, kBM) ||
+        !make_head_tile_map(&mk, k16, P.total, P.h_kv, kBN) ||
         !make_head_tile_map(&mdo, dout, P.total, P.h_q, kBM) ||
         !make_f32_head_half_map(&mdq, acc, P.total, P.h_q, kBM))
         return cudaErrorInvalidValue;
     // the register split is only safe at exactly this launch value
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
+    e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(BwdSmem) + 1024;
@@ -594,7 +616,7 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
     e = cudaMemsetAsync(acc, 0, n * sizeof(float), st);
     if (e != cudaSuccess) return e;
     dim3 grid((P.max_seqlen + kBN - 1) / kBN, P.h_kv, P.nseq);
-    bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k,
+    bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k16,
                                                 (const __nv_bfloat16*)v, lse, delta,
                                                 (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, flags);
     count_launches(1);

@@ -97,7 +97,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const int rb = gridDim.x - 1 - blockIdx.x;  // longest row blocks first
     const int h = blockIdx.y, seq = blockIdx.z;
     int start, L;
-    seq_bounds(P, seq, start, L);
+    if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     const int r0 = rb * kB;
     if (r0 >= L) return;  // uniform for the CTA, before any barrier or tensor memory
     int kb_lo = 0, kb_hi = (L - 1) / kB;
@@ -167,7 +167,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const int hi = P.causal ? min(row, L - 1) : L - 1;
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, i & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, i & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float p[128];
@@ -198,7 +198,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 p[j] = fast_exp2(x0);
                 p[j + 1] = fast_exp2(x1);
             }
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, i & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, i & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             uint32_t dsw[64];
@@ -220,7 +220,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             }
             if (i > 0) {
                 // dQ of the previous block has read the dS columns
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.dq_done, (i - 1) & 1, flags, abort_word));
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.dq_done, (i - 1) & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -229,7 +229,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             tc_fence_before();
             mbar_arrive(&sm.ds_full);
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.dq_done, (nblk - 1) & 1, flags, abort_word));
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.dq_done, (nblk - 1) & 1, flags, abort_word, P.wait_ns));
         if (ok) {
             tc_fence_after();
             uint4* dst = reinterpret_cast<uint4*>(dq + ((size_t)(start + row) * P.h_q + h) * kD);
@@ -265,7 +265,7 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             for (int i = 0; i < nblk; ++i) {
                 const int st = i % kAStages;
                 if (i >= kAStages &&
-                    !wait_phase(&sm.kv_empty[st], ((i / kAStages) - 1) & 1, flags, abort_word))
+                    !wait_phase(&sm.kv_empty[st], ((i / kAStages) - 1) & 1, flags, abort_word, P.wait_ns))
                     break;
                 const int kpos = start + (kb_lo + i) * kB;
                 mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
@@ -277,11 +277,11 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
                 issued = i + 1;
             }
             // copies still in flight must land before the CTA's shared memory goes away
-            drain_phase(&sm.do_full, 0);
+            drain_phase(&sm.do_full, 0, P.wait_ns);
             for (int i = max(0, issued - kAStages); i < issued; ++i) {
                 const int st = i % kAStages;
-                drain_phase(&sm.k_full[st], (i / kAStages) & 1);
-                drain_phase(&sm.v_full[st], (i / kAStages) & 1);
+                drain_phase(&sm.k_full[st], (i / kAStages) & 1, P.wait_ns);
+                drain_phase(&sm.v_full[st], (i / kAStages) & 1, P.wait_ns);
             }
         }
     } else if (lane == 0) {
@@ -307,14 +307,14 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             for (int kk = 0; kk < kB / 16; ++kk)
                 mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, dk + mnstep_off(0, kk), idQ, acc || kk > 0);
         };
-        bool ok = wait_phase(&sm.q_ready, 0, flags, abort_word) &&
-                  wait_phase(&sm.k_full[0], 0, flags, abort_word);
+        bool ok = wait_phase(&sm.q_ready, 0, flags, abort_word, P.wait_ns) &&
+                  wait_phase(&sm.k_full[0], 0, flags, abort_word, P.wait_ns);
         if (ok) {
             tc_fence_after();
             s_product(0);
             mma_commit(&sm.s_full);
-            ok = wait_phase(&sm.do_full, 0, flags, abort_word) &&
-                 wait_phase(&sm.v_full[0], 0, flags, abort_word);
+            ok = wait_phase(&sm.do_full, 0, flags, abort_word, P.wait_ns) &&
+                 wait_phase(&sm.v_full[0], 0, flags, abort_word, P.wait_ns);
         }
         if (ok) {
             tc_fence_after();
@@ -325,25 +325,25 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             const int st = i % kAStages, st1 = (i + 1) % kAStages;
             if (i + 1 < nblk) {
                 // S(i+1) once S(i) is read, dP(i+1) once dP(i) is read: both ahead of dQ(i)
-                if (!(ok = wait_phase(&sm.s_loaded, i & 1, flags, abort_word))) break;
-                if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kAStages) & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.s_loaded, i & 1, flags, abort_word, P.wait_ns))) break;
+                if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kAStages) & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 s_product(st1);
                 mma_commit(&sm.s_full);
-                if (!(ok = wait_phase(&sm.dp_loaded, i & 1, flags, abort_word))) break;
-                if (!(ok = wait_phase(&sm.v_full[st1], ((i + 1) / kAStages) & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.dp_loaded, i & 1, flags, abort_word, P.wait_ns))) break;
+                if (!(ok = wait_phase(&sm.v_full[st1], ((i + 1) / kAStages) & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 dp_product(st1);
                 mma_commit(&sm.dp_full);
             }
-            if (!(ok = wait_phase(&sm.ds_full, i & 1, flags, abort_word))) break;
+            if (!(ok = wait_phase(&sm.ds_full, i & 1, flags, abort_word, P.wait_ns))) break;
             tc_fence_after();
             dq_product(st, i > 0);
             mma_commit(&sm.dq_done);
             mma_commit(&sm.kv_empty[st]);  // K(i) and V(i) are no longer read
         }
         mma_commit(&sm.drained);
-        drain_phase(&sm.drained, 0);
+        drain_phase(&sm.drained, 0, P.wait_ns);
     }
     tc_fence_before();
     __syncthreads();
@@ -384,7 +384,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int kb = blockIdx.x, hk = blockIdx.y, seq = blockIdx.z;
     int start, L;
-    seq_bounds(P, seq, start, L);
+    if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     const int j0 = kb * kB;
     if (j0 >= L) return;  // uniform for the CTA
     // query blocks that see some key of this block
@@ -434,9 +434,9 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const int st = i % kBStages;
             const int qb = qb_lo + i % nqb;
             const int rbase = qb * kB + g * 64;  // first query row of this thread's columns
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.rows_full[st], (i / kBStages) & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.rows_full[st], (i / kBStages) & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, i & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full, i & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float p[64];
@@ -478,7 +478,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     if (!seen) p[c] = 0.f;
                 }
             }
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, i & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.dp_full, i & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             uint32_t pw[32], dw[32];
@@ -502,7 +502,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             if (i > 0) {
                 // dV and dK of the previous step have read P^T and dS^T
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.pd_free, (i - 1) & 1, flags, abort_word));
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.pd_free, (i - 1) & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -512,7 +512,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tc_fence_before();
             mbar_arrive(&sm.ds_full);
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.acc_done, 0, flags, abort_word));
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(&sm.acc_done, 0, flags, abort_word, P.wait_ns));
         if (ok) {
             tc_fence_after();
             // warpgroup g writes columns [64 g, 64 g + 64) of dV and dK
@@ -566,7 +566,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const int st = i % kBStages;
             if (i >= kBStages &&
                 !__all_sync(0xffffffffu, wait_phase(&sm.q_empty[st], ((i / kBStages) - 1) & 1, flags,
-                                                    abort_word)))
+                                                    abort_word, P.wait_ns)))
                 break;
             const int hq = hk * P.group + i / nqb;
             const int r0 = (qb_lo + i % nqb) * kB;
@@ -589,9 +589,9 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             issued = i + 1;
         }
         if (lane == 0) {
-            drain_phase(&sm.kv_full, 0);
+            drain_phase(&sm.kv_full, 0, P.wait_ns);
             for (int i = max(0, issued - kBStages); i < issued; ++i)
-                drain_phase(&sm.q_full[i % kBStages], (i / kBStages) & 1);
+                drain_phase(&sm.q_full[i % kBStages], (i / kBStages) & 1, P.wait_ns);
         }
     } else if (lane == 0) {
         // ------------------------------------------------------------ MMA issuer
@@ -621,13 +621,13 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             for (int kk = 0; kk < kB / 16; ++kk)
                 mma_ts(tmem + kColDK, tmem + kColDST + kk * 8, dqm + mnstep_off(0, kk), idG, acc || kk > 0);
         };
-        bool ok = wait_phase(&sm.kv_full, 0, flags, abort_word) &&
-                  wait_phase(&sm.q_full[0], 0, flags, abort_word);
+        bool ok = wait_phase(&sm.kv_full, 0, flags, abort_word, P.wait_ns) &&
+                  wait_phase(&sm.q_full[0], 0, flags, abort_word, P.wait_ns);
         if (ok) {
             tc_fence_after();
             st_product(0);
             mma_commit(&sm.s_full);
-            ok = wait_phase(&sm.s_loaded, 0, flags, abort_word);
+            ok = wait_phase(&sm.s_loaded, 0, flags, abort_word, P.wait_ns);
         }
         if (ok) {
             tc_fence_after();
@@ -638,19 +638,19 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const int st = i % kBStages, st1 = (i + 1) % kBStages;
             if (i + 1 < nsteps) {
                 // S^T(i+1) over dP^T(i) once that has been read, ahead of dV/dK(i)
-                if (!(ok = wait_phase(&sm.dp_loaded, i & 1, flags, abort_word))) break;
-                if (!(ok = wait_phase(&sm.q_full[st1], ((i + 1) / kBStages) & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.dp_loaded, i & 1, flags, abort_word, P.wait_ns))) break;
+                if (!(ok = wait_phase(&sm.q_full[st1], ((i + 1) / kBStages) & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 st_product(st1);
                 mma_commit(&sm.s_full);
             }
-            if (!(ok = wait_phase(&sm.ds_full, i & 1, flags, abort_word))) break;
+            if (!(ok = wait_phase(&sm.ds_full, i & 1, flags, abort_word, P.wait_ns))) break;
             tc_fence_after();
             grads(st, i > 0);
             mma_commit(&sm.pd_free);
             mma_commit(&sm.q_empty[st]);
             if (i + 1 < nsteps) {
-                if (!(ok = wait_phase(&sm.s_loaded, (i + 1) & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.s_loaded, (i + 1) & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 dpt_product(st1);
                 mma_commit(&sm.dp_full);
@@ -658,7 +658,7 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mma_commit(&sm.acc_done);
         mma_commit(&sm.drained);
-        drain_phase(&sm.drained, 0);
+        drain_phase(&sm.drained, 0, P.wait_ns);
     }
     tc_fence_before();
     __syncthreads();

@@ -1,6 +1,7 @@
 // tc_common.cuh - pieces shared by the tensor-core kernels: bounded mbarrier
 // waits driven by the global nanosecond timer, and the TMA tensor-map builder
-// for [T, H, 64] bf16 tensors.
+// for [T, H, 64] bf16 tensors. The wait limit is a kernel argument
+// (Problem::wait_ns, 2 s unless a test lowers it).
 #pragma once
 
 #include <cuda.h>
@@ -12,8 +13,6 @@
 namespace sinkattn {
 namespace tc {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -24,13 +23,13 @@ __device__ __forceinline__ uint64_t now_ns() {
 // the CTA abort word. Returns false if the wait did not complete (timeout, or
 // another role of the CTA already gave up).
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint32_t* flags,
-                                           volatile int* abort_word) {
+                                           volatile int* abort_word, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = now_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_word) return false;
-        if (now_ns() - t0 > kWaitLimitNs) {
+        if (now_ns() - t0 > limit_ns) {
             atomicOr(flags, kFlagTimeout);
             *abort_word = 1;
             return false;
@@ -41,9 +40,9 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint3
 // Time-bounded wait that ignores the abort word: used only to let copies or
 // MMAs that were already issued finish before shared or tensor memory is
 // given up.
-__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = now_ns();
-    while (!mbar_try_wait(bar, parity) && now_ns() - t0 < kWaitLimitNs) {
+    while (!mbar_try_wait(bar, parity) && now_ns() - t0 < limit_ns) {
     }
 }
 

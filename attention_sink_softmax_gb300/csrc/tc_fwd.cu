@@ -21,13 +21,20 @@
 //                  holding back the other tile's products; a K/V stage is
 //                  refilled once every tile's issuer is done with it.
 //   warps 4t..4t+3 softmax of tile t: thread r owns row r (tensor-memory lane
-//                  r). The running max starts at the sink logit and the running
-//                  sum at the sink's own term, so the sink joins the
-//                  denominator and contributes no value row. The max is only
-//                  moved (and O rescaled in tensor memory) when it grows by
-//                  more than kRescaleLog2 in log2 units; P values then stay
-//                  below 2^kRescaleLog2 and the final O / l is unchanged.
-// Tensor memory (512 columns): S_t at t*128, O_t at 256 + t*64, P_t (bf16
+//                  r). An online softmax over the keys (running max and sum);
+//                  once every key is seen, the sink's term joins the
+//                  denominator relative to the larger of the keys' max and the
+//                  sink logit (fold_sink), and it contributes no value row.
+//                  The max is only moved (and O rescaled in tensor memory)
+//                  when it grows by more than kRescaleLog2 in log2 units; P
+//                  values then stay below 2^kRescaleLog2 and the final O / l
+//                  is unchanged.
+// P V runs in f16, not bf16: P lies in [0, 2^kRescaleLog2], where f16 keeps
+// 11 bits against bf16's 8, and the product's rounding of P is what limits the
+// accuracy of O (and of D = dO . O in the backward) when logits are large. One
+// product's A and B share a format, so V is read from an f16 copy that
+// tc_fwd writes into the workspace first (convert.cu; exact for |V| <= 65504).
+// Tensor memory (512 columns): S_t at t*128, O_t at 256 + t*64, P_t (f16
 // pairs) at 384 + t*64. Every mbarrier wait is bounded; a wait that gives up
 // sets the timeout flag and the CTA winds down without further work.
 //
@@ -69,6 +76,45 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 384 * kLaunchRegs, "r
 template <int NT>
 constexpr int fwd_threads() { return NT * 128 + 128; }
 
+// Eight consecutive O values of a row, scaled by 1 / l, stored as bf16 at dst;
+// when dst_lo is given, the bf16 of what that rounding dropped (O - bf16(O),
+// exact in fp32) goes to dst_lo, so that o + o_lo carries about 16 bits of O.
+__device__ __forceinline__ void store_o8(uint4* dst, uint4* dst_lo, const uint32_t* a, float inv) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(a[j]) * inv;
+    uint32_t hi[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+    *dst = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    if (dst_lo) {
+        uint32_t lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            lo[j] = pack_bf16x2(x[2 * j] - __uint_as_float(hi[j] << 16),
+                                x[2 * j + 1] - __uint_as_float(hi[j] & 0xFFFF0000u));
+        *dst_lo = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// The sink's term joins the row's denominator once every key has been seen:
+// with the keys' running max m and sum l (log2 units, l relative to m) and the
+// sink logit s2 = S_h log2 e, both parts are taken relative to M = max(m, s2):
+//   l_tot = l 2^(m - M) + 2^(s2 - M),  O = acc 2^(m - M) / l_tot,
+//   LSE = (M + log2 l_tot) ln 2.
+// The sink adds no value row. Keeping it out of the running max keeps P (the
+// operand of the f16 P V product) relative to the largest key, so a row whose
+// sink dominates every key (P_ij ~ e^-30) still has P values f16 can hold.
+// Returns the factor that turns acc into O; writes the row's LSE to *lse_out.
+__device__ __forceinline__ float fold_sink(float m, float l, float s2, float* lse_out) {
+    const float M = fmaxf(m, s2);
+    const float a = m == -INFINITY ? 0.f : fast_exp2(m - M);
+    const float st = s2 == -INFINITY ? 0.f : fast_exp2(s2 - M);
+    const float lt = l * a + st;
+    *lse_out = (M + __log2f(lt)) * kLn2;
+    return lt > 0.f ? a / lt : 0.f;
+}
+
 template <int NT, int D>
 struct FwdSmem {
     alignas(1024) __nv_bfloat16 q[NT][kBM * D];  // D/64 atoms of 128 rows x 64
@@ -91,7 +137,7 @@ __global__ void __launch_bounds__(fwd_threads<NT>(), 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
-              float* __restrict__ lse, uint32_t* flags) {
+              __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, uint32_t* flags) {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(D == 64 || NT == 1, "tensor memory holds one D = 128 tile");
     constexpr int kAtoms = D / kAtomCols;
@@ -104,7 +150,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int seq = blockIdx.z;
     const int h0 = blockIdx.y * NT;
     int start, L;
-    seq_bounds(P, seq, start, L);
+    if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && L > P.max_seqlen) atomicOr(flags, kFlagSeqTooLong);
     const int r0 = rb * kBM;
     if (r0 >= L) return;  // uniform for the whole CTA, before any barrier or TMEM use
@@ -156,11 +202,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t tO = tmem + lane_off + 256 + t * 64;
         const uint32_t tP = tmem + lane_off + 384 + t * 64;
         const float sc = P.scale_log2;
-        float m = __ldg(sinks + h) * kLog2e;  // running max in log2 units, seeded by the sink
-        float l = m == -INFINITY ? 0.f : 1.f;  // running sum, seeded by the sink's own term
+        const float sink2 = __ldg(sinks + h) * kLog2e;  // S_h in log2 units
+        float m = -INFINITY;  // the keys' running max in log2 units
+        float l = 0.f;        // the keys' running sum relative to m (the sink joins at the end)
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], i & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], i & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float s[128];
@@ -213,10 +260,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // special-function units at once.
             if (NT == 2 && (t == 1 || i > 0)) {
                 const int ph = t == 0 ? i - 1 : i;
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word));
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
             }
-            // P into registers first (bf16 pairs): the exponentials overlap the
+            // P into registers first (f16 pairs): the exponentials overlap the
             // previous block's P V product, which still reads P_t and writes O_t
             uint32_t pk[64];
 #pragma unroll
@@ -226,12 +273,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const float p0 = fast_exp2(x0);
                 const float p1 = fast_exp2(x1);
                 rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
-                pk[j >> 1] = pack_bf16x2(p0, p1);
+                pk[j >> 1] = pack_f16x2(p0, p1);
             }
             if (NT == 2) mbar_arrive(&sm.exp_turn[(1 - t) % NT]);
             if (i > 0) {
                 ok = __all_sync(0xffffffffu,
-                                wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word));
+                                wait_phase(&sm.o_done[t], (i - 1) & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -266,13 +313,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         if (ok)
             ok = __all_sync(0xffffffffu,
-                            wait_phase(&sm.o_done[t], (nblk - 1) & 1, flags, abort_word));
+                            wait_phase(&sm.o_done[t], (nblk - 1) & 1, flags, abort_word, P.wait_ns));
         if (ok) {
             tc_fence_after();
-            const float inv = 1.f / l;
-            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * D);
+            float row_lse;
+            const float inv = fold_sink(m, l, sink2, &row_lse);
+            const size_t ooff = ((size_t)(start + row) * P.h_q + h) * D;
+            uint4* dst = reinterpret_cast<uint4*>(out + ooff);
+            uint4* dst_lo = out_lo ? reinterpret_cast<uint4*>(out_lo + ooff) : nullptr;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 64) {
+                // both loads complete before any register they write is read
                 uint32_t oa[32], ob[32];
                 tmem_ld32(tO + c0, oa);
                 tmem_ld32(tO + c0 + 32, ob);
@@ -280,27 +331,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (valid) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(oa[8 * j + 0]) * inv, __uint_as_float(oa[8 * j + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(oa[8 * j + 2]) * inv, __uint_as_float(oa[8 * j + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(oa[8 * j + 4]) * inv, __uint_as_float(oa[8 * j + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(oa[8 * j + 6]) * inv, __uint_as_float(oa[8 * j + 7]) * inv);
-                        dst[c0 / 8 + j] = w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(ob[8 * j + 0]) * inv, __uint_as_float(ob[8 * j + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(ob[8 * j + 2]) * inv, __uint_as_float(ob[8 * j + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(ob[8 * j + 4]) * inv, __uint_as_float(ob[8 * j + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(ob[8 * j + 6]) * inv, __uint_as_float(ob[8 * j + 7]) * inv);
-                        dst[c0 / 8 + 4 + j] = w;
+                        store_o8(dst + c0 / 8 + j, dst_lo ? dst_lo + c0 / 8 + j : nullptr, oa + 8 * j, inv);
+                        store_o8(dst + c0 / 8 + 4 + j, dst_lo ? dst_lo + c0 / 8 + 4 + j : nullptr, ob + 8 * j, inv);
                     }
                 }
             }
-            if (valid) {
-                lse[(size_t)h * P.total + start + row] = (m + __log2f(l)) * kLn2;
-            }
+            if (valid) lse[(size_t)h * P.total + start + row] = row_lse;
         }
         } else {
         if (NT == 2) regs_decrease<kOtherRegs>();
@@ -318,8 +354,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 int issued = 0;
                 for (int i = 0; i < nblk; ++i) {
                     const int st = i % kStages;
+                    // test hook (off unless a test sets it): no load after the first
+                    // stage, so the consumers' bounded waits run out
+                    if (P.withhold_load && i == 1) break;
                     if (i >= kStages &&
-                        !wait_phase(&sm.kv_empty[st], ((i / kStages) - 1) & 1, flags, abort_word))
+                        !wait_phase(&sm.kv_empty[st], ((i / kStages) - 1) & 1, flags, abort_word, P.wait_ns))
                         break;
                     const int kpos = start + (kb_lo + i) * kBN;
                     mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
@@ -333,11 +372,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     issued = i + 1;
                 }
                 // copies still in flight must land before the CTA's shared memory goes away
-                drain_phase(&sm.q_full, 0);
+                drain_phase(&sm.q_full, 0, P.wait_ns);
                 for (int i = max(0, issued - kStages); i < issued; ++i) {
                     const int st = i % kStages;
-                    drain_phase(&sm.k_full[st], (i / kStages) & 1);
-                    drain_phase(&sm.v_full[st], (i / kStages) & 1);
+                    drain_phase(&sm.k_full[st], (i / kStages) & 1, P.wait_ns);
+                    drain_phase(&sm.v_full[st], (i / kStages) & 1, P.wait_ns);
                 }
             }
         } else if (warp >= 4 * NT + 1 && warp <= 4 * NT + NT && lane == 0) {
@@ -346,7 +385,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);       // Q, K both K-major
             // P from TMEM, V MN-major with N = D: at D = 128 the two 64-column
             // atoms are 16 KB apart (the descriptor's leading byte offset)
-            constexpr uint32_t idO = idesc_bf16(kBM, D, 0, 1);
+            constexpr uint32_t idO = idesc_f16(kBM, D, 0, 1);  // P and V in f16
             const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
             // K step kk of S reads atom kk / 4 at byte offset 32 (kk % 4); both are
             // added to the descriptors' start-address field (16-byte units)
@@ -359,8 +398,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     mma_ss(tS, dq + off, dk + off, idS, kk > 0);
                 }
             };
-            bool ok = wait_phase(&sm.q_full, 0, flags, abort_word) &&
-                      wait_phase(&sm.k_full[0], 0, flags, abort_word);
+            bool ok = wait_phase(&sm.q_full, 0, flags, abort_word, P.wait_ns) &&
+                      wait_phase(&sm.k_full[0], 0, flags, abort_word, P.wait_ns);
             if (ok) {
                 tc_fence_after();
                 s_product(0);
@@ -371,16 +410,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int st1 = (i + 1) % kStages;
                 if (i + 1 < nblk) {
                     // S_t(i+1) = Q_t K(i+1)^T as soon as S_t(i) has been read
-                    if (!(ok = wait_phase(&sm.s_loaded[t], i & 1, flags, abort_word))) break;
-                    if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word)))
+                    if (!(ok = wait_phase(&sm.s_loaded[t], i & 1, flags, abort_word, P.wait_ns))) break;
+                    if (!(ok = wait_phase(&sm.k_full[st1], ((i + 1) / kStages) & 1, flags, abort_word, P.wait_ns)))
                         break;
                     tc_fence_after();
                     s_product(st1);
                     mma_commit(&sm.s_full[t]);
                 }
                 // O_t += P_t(i) V(i)
-                if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word))) break;
-                if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word))) break;
+                if (!(ok = wait_phase(&sm.p_full[t], i & 1, flags, abort_word, P.wait_ns))) break;
+                if (!(ok = wait_phase(&sm.v_full[st], (i / kStages) & 1, flags, abort_word, P.wait_ns))) break;
                 tc_fence_after();
                 const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), kAtomBytes, 1024);
 #pragma unroll
@@ -392,7 +431,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             // every MMA issued above must finish before tensor memory is released
             mma_commit(&sm.drained[t]);
-            drain_phase(&sm.drained[t], 0);
+            drain_phase(&sm.drained[t], 0, P.wait_ns);
         }
     }
     tc_fence_before();
@@ -437,7 +476,7 @@ __global__ void __launch_bounds__(fwd_threads<NT>(), 1)
 fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
-              float* __restrict__ lse, uint32_t* flags) {
+              __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, uint32_t* flags) {
     constexpr int D = 64;
     constexpr int kTiles = kWindowTiles;
     constexpr int kQBufs = 2;
@@ -451,7 +490,7 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int seq = blockIdx.z;
     const int h0 = blockIdx.y * NT;
     int start, L;
-    seq_bounds(P, seq, start, L);
+    if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && L > P.max_seqlen) atomicOr(flags, kFlagSeqTooLong);
     // this CTA's row tiles: row blocks rb0 .. rb0 + ntile - 1 of the sequence
     const int rb0 = cb * kTiles;
@@ -520,10 +559,10 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         tile_blocks(k, r0, kb_lo, nblk);
         const int row = r0 + r;
         const bool valid = row < L;
-        float m = sink2;                       // running max in log2 units, seeded by the sink
-        float l = m == -INFINITY ? 0.f : 1.f;  // running sum, seeded by the sink's own term
+        float m = -INFINITY;  // the keys' running max in log2 units
+        float l = 0.f;        // the keys' running sum relative to m (the sink joins at the end)
         for (int i = 0; i < nblk; ++i, ++g) {
-            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], g & 1, flags, abort_word));
+            ok = __all_sync(0xffffffffu, wait_phase(&sm.s_full[t], g & 1, flags, abort_word, P.wait_ns));
             if (!ok) break;
             tc_fence_after();
             float s[128];
@@ -576,10 +615,10 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // special-function units at once.
             if (NT == 2 && (t == 1 || g > 0)) {
                 const int ph = t == 0 ? g - 1 : g;
-                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word));
+                ok = __all_sync(0xffffffffu, wait_phase(&sm.exp_turn[t], ph & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
             }
-            // P into registers first (bf16 pairs): the exponentials overlap the
+            // P into registers first (f16 pairs): the exponentials overlap the
             // previous block's P V product, which still reads P_t and writes O_t
             uint32_t pk[64];
 #pragma unroll
@@ -589,13 +628,13 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const float p0 = fast_exp2(x0);
                 const float p1 = fast_exp2(x1);
                 rs2[(j >> 1) & 3] = f2_add(rs2[(j >> 1) & 3], f2_pack(p0, p1));
-                pk[j >> 1] = pack_bf16x2(p0, p1);
+                pk[j >> 1] = pack_f16x2(p0, p1);
             }
             if (NT == 2) mbar_arrive(&sm.exp_turn[(1 - t) % NT]);
             if (g > 0) {
                 // P_t V of the previous block (possibly the previous tile's) is done with P_t
                 ok = __all_sync(0xffffffffu,
-                                wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word));
+                                wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word, P.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -629,35 +668,31 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             m = m_new;
         }
         if (!ok) break;
-        ok = __all_sync(0xffffffffu, wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word));
+        ok = __all_sync(0xffffffffu, wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word, P.wait_ns));
         if (!ok) break;
         {
             tc_fence_after();
-            const float inv = 1.f / l;
-            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(start + row) * P.h_q + h) * D);
-            uint32_t o_all[D];
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t oa[32];
-                tmem_ld32(tO + c0, oa);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o_all[c0 + j] = oa[j];
-            }
+            float row_lse;
+            const float inv = fold_sink(m, l, sink2, &row_lse);
+            const size_t ooff = ((size_t)(start + row) * P.h_q + h) * D;
+            uint4* dst = reinterpret_cast<uint4*>(out + ooff);
+            uint4* dst_lo = out_lo ? reinterpret_cast<uint4*>(out_lo + ooff) : nullptr;
+            static_assert(D == 64, "the multi-tile forward is 64 wide");
+            // both loads complete before any register they write is read
+            uint32_t oa[32], ob[32];
+            tmem_ld32(tO, oa);
+            tmem_ld32(tO + 32, ob);
             tmem_ld_wait();
             // O_t is in registers: the next tile's first P V may overwrite it
             tc_fence_before();
             mbar_arrive(&sm.o_free[t]);
             if (valid) {
 #pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(o_all[8 * j + 0]) * inv, __uint_as_float(o_all[8 * j + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(o_all[8 * j + 2]) * inv, __uint_as_float(o_all[8 * j + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(o_all[8 * j + 4]) * inv, __uint_as_float(o_all[8 * j + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(o_all[8 * j + 6]) * inv, __uint_as_float(o_all[8 * j + 7]) * inv);
-                    dst[j] = w;
+                for (int j = 0; j < 4; ++j) {
+                    store_o8(dst + j, dst_lo ? dst_lo + j : nullptr, oa + 8 * j, inv);
+                    store_o8(dst + 4 + j, dst_lo ? dst_lo + 4 + j : nullptr, ob + 8 * j, inv);
                 }
-                lse[(size_t)h * P.total + start + row] = (m + __log2f(l)) * kLn2;
+                lse[(size_t)h * P.total + start + row] = row_lse;
             }
         }
         }  // tiles
@@ -677,7 +712,7 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     const int qb = k % kQBufs;
                     // the buffer's previous tile: every S product that read it has completed
                     if (k >= kQBufs &&
-                        !wait_phase(&sm.q_empty[qb], ((k / kQBufs) - 1) & 1, flags, abort_word))
+                        !wait_phase(&sm.q_empty[qb], ((k / kQBufs) - 1) & 1, flags, abort_word, P.wait_ns))
                         break;
                     mbar_arrive_expect_tx(&sm.q_full[qb], NT * kTileBytes);
                     for (int t = 0; t < NT; ++t)
@@ -688,7 +723,7 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     for (int i = 0; i < nblk; ++i, ++g) {
                         const int st = g % kStages;
                         if (g >= kStages &&
-                            !wait_phase(&sm.kv_empty[st], ((g / kStages) - 1) & 1, flags, abort_word)) {
+                            !wait_phase(&sm.kv_empty[st], ((g / kStages) - 1) & 1, flags, abort_word, P.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -706,11 +741,11 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 // copies still in flight must land before the CTA's shared memory goes away
                 for (int k = max(0, q_issued - kQBufs); k < q_issued; ++k)
-                    drain_phase(&sm.q_full[k % kQBufs], (k / kQBufs) & 1);
+                    drain_phase(&sm.q_full[k % kQBufs], (k / kQBufs) & 1, P.wait_ns);
                 for (int j = max(0, issued - kStages); j < issued; ++j) {
                     const int st = j % kStages;
-                    drain_phase(&sm.k_full[st], (j / kStages) & 1);
-                    drain_phase(&sm.v_full[st], (j / kStages) & 1);
+                    drain_phase(&sm.k_full[st], (j / kStages) & 1, P.wait_ns);
+                    drain_phase(&sm.v_full[st], (j / kStages) & 1, P.wait_ns);
                 }
             }
         } else if (warp >= 4 * NT + 1 && warp <= 4 * NT + NT && lane == 0) {
@@ -719,7 +754,7 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             constexpr uint32_t idS = idesc_bf16(kBM, kBN, 0, 0);       // Q, K both K-major
             // P from TMEM, V MN-major with N = D: at D = 128 the two 64-column
             // atoms are 16 KB apart (the descriptor's leading byte offset)
-            constexpr uint32_t idO = idesc_bf16(kBM, D, 0, 1);
+            constexpr uint32_t idO = idesc_f16(kBM, D, 0, 1);  // P and V in f16
             const uint32_t tS = tmem + t * 128, tO = tmem + 256 + t * 64, tP = tmem + 384 + t * 64;
             // S_t = Q_t K^T from Q buffer qb and K stage st. K step kk reads atom
             // kk / 4 at byte offset 32 (kk % 4); both are added to the
@@ -737,8 +772,8 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             };
             int r0, kb_lo, nblk;
             tile_blocks(0, r0, kb_lo, nblk);
-            bool ok = wait_phase(&sm.q_full[0], 0, flags, abort_word) &&
-                      wait_phase(&sm.k_full[0], 0, flags, abort_word);
+            bool ok = wait_phase(&sm.q_full[0], 0, flags, abort_word, P.wait_ns) &&
+                      wait_phase(&sm.k_full[0], 0, flags, abort_word, P.wait_ns);
             if (ok) {
                 tc_fence_after();
                 s_product(0, 0);
@@ -756,17 +791,17 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     // as soon as S_t of this block has been read
                     const bool next_here = i + 1 < nblk;
                     if (next_here || k + 1 < ntile) {
-                        if (!(ok = wait_phase(&sm.s_loaded[t], g & 1, flags, abort_word))) break;
+                        if (!(ok = wait_phase(&sm.s_loaded[t], g & 1, flags, abort_word, P.wait_ns))) break;
                         int nqb = qb, last_of_tile = i + 2 == nblk;
                         if (!next_here) {
                             int nr0, nkb_lo, nnblk;
                             tile_blocks(k + 1, nr0, nkb_lo, nnblk);
                             nqb = (k + 1) % kQBufs;
                             last_of_tile = nnblk == 1;
-                            if (!(ok = wait_phase(&sm.q_full[nqb], ((k + 1) / kQBufs) & 1, flags, abort_word)))
+                            if (!(ok = wait_phase(&sm.q_full[nqb], ((k + 1) / kQBufs) & 1, flags, abort_word, P.wait_ns)))
                                 break;
                         }
-                        if (!(ok = wait_phase(&sm.k_full[st1], ((g + 1) / kStages) & 1, flags, abort_word)))
+                        if (!(ok = wait_phase(&sm.k_full[st1], ((g + 1) / kStages) & 1, flags, abort_word, P.wait_ns)))
                             break;
                         tc_fence_after();
                         s_product(nqb, st1);
@@ -776,9 +811,9 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                     // O_t += P_t(g) V(g); the first block of a tile overwrites O_t,
                     // which the softmax has read for the previous tile
-                    if (!(ok = wait_phase(&sm.p_full[t], g & 1, flags, abort_word))) break;
-                    if (!(ok = wait_phase(&sm.v_full[st], (g / kStages) & 1, flags, abort_word))) break;
-                    if (i == 0 && k > 0 && !(ok = wait_phase(&sm.o_free[t], (k - 1) & 1, flags, abort_word)))
+                    if (!(ok = wait_phase(&sm.p_full[t], g & 1, flags, abort_word, P.wait_ns))) break;
+                    if (!(ok = wait_phase(&sm.v_full[st], (g / kStages) & 1, flags, abort_word, P.wait_ns))) break;
+                    if (i == 0 && k > 0 && !(ok = wait_phase(&sm.o_free[t], (k - 1) & 1, flags, abort_word, P.wait_ns)))
                         break;
                     tc_fence_after();
                     const uint64_t dv = smem_desc_sw128(smem_u32(sm.v[st]), kAtomBytes, 1024);
@@ -792,7 +827,7 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             // every MMA issued above must finish before tensor memory is released
             mma_commit(&sm.drained[t]);
-            drain_phase(&sm.drained[t], 0);
+            drain_phase(&sm.drained[t], 0, P.wait_ns);
         }
     }
     tc_fence_before();
@@ -853,12 +888,15 @@ bool tc_fwd_supported(const Problem& P, bool bf16) {
     return bf16 && (P.head_dim == 64 || P.head_dim == 128) && encode_fn() != nullptr && P.total > 0;
 }
 
-size_t tc_fwd_workspace_bytes(const Problem&, bool) { return 0; }
+// the f16 copy of V
+size_t tc_fwd_workspace_bytes(const Problem& P, bool bf16) {
+    return bf16 ? (size_t)P.total * P.h_kv * P.head_dim * 2 : 0;
+}
 
 template <int NT, int D>
 static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
-                              const CUtensorMap& mv, const float* sinks, void* o, float* lse,
-                              uint32_t* flags, cudaStream_t st) {
+                              const CUtensorMap& mv, const float* sinks, void* o, void* o_lo,
+                              float* lse, uint32_t* flags, cudaStream_t st) {
     if (NT == 2) {
         // the register split above is only safe at exactly this launch value
         cudaFuncAttributes fa;
@@ -871,16 +909,16 @@ static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUt
         fwd_tc_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid((P.max_seqlen + kBM - 1) / kBM, P.h_q / NT, P.nseq);
-    fwd_tc_kernel<NT, D><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
-                                                            (__nv_bfloat16*)o, lse, flags);
+    fwd_tc_kernel<NT, D><<<grid, fwd_threads<NT>(), smem, st>>>(
+        mq, mk, mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
     count_launches(1);
     return cudaGetLastError();
 }
 
 template <int NT>
 static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
-                                    const CUtensorMap& mv, const float* sinks, void* o, float* lse,
-                                    uint32_t* flags, cudaStream_t st) {
+                                    const CUtensorMap& mv, const float* sinks, void* o, void* o_lo,
+                                    float* lse, uint32_t* flags, cudaStream_t st) {
     if (NT == 2) {
         // the register split above is only safe at exactly this launch value
         cudaFuncAttributes fa;
@@ -894,28 +932,32 @@ static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, con
     if (attr_err != cudaSuccess) return attr_err;
     const int nrb = (P.max_seqlen + kBM - 1) / kBM;
     dim3 grid((nrb + kWindowTiles - 1) / kWindowTiles, P.h_q / NT, P.nseq);
-    fwd_tc_tiles_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(mq, mk, mv, P, sinks,
-                                                               (__nv_bfloat16*)o, lse, flags);
+    fwd_tc_tiles_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(
+        mq, mk, mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
     count_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
-                   const float* sinks, void* o, float* lse, uint32_t* flags, void*,
-                   cudaStream_t st) {
+                   const float* sinks, void* o, void* o_lo, float* lse, uint32_t* flags,
+                   void* workspace, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
+    // V in f16 for the P V product (the same 2-byte layout; TMA copies bytes)
+    void* v16 = workspace;
+    cudaError_t e = convert_bf16_to_f16(v, v16, (size_t)P.total * P.h_kv * P.head_dim, st);
+    if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv;
     if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM, P.head_dim) ||
         !make_head_tile_map(&mk, k, P.total, P.h_kv, kBN, P.head_dim) ||
-        !make_head_tile_map(&mv, v, P.total, P.h_kv, kBN, P.head_dim))
+        !make_head_tile_map(&mv, v16, P.total, P.h_kv, kBN, P.head_dim))
         return cudaErrorInvalidValue;
-    if (P.head_dim == 128) return launch_fwd<1, 128>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    if (P.head_dim == 128) return launch_fwd<1, 128>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     if (P.causal && P.window > 0 && P.window <= 2 * kBN) {
-        if (P.group % 2 == 0) return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, lse, flags, st);
-        return launch_fwd_tiles<1>(P, mq, mk, mv, sinks, o, lse, flags, st);
+        if (P.group % 2 == 0) return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
+        return launch_fwd_tiles<1>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     }
-    if (P.group % 2 == 0) return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
-    return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, lse, flags, st);
+    if (P.group % 2 == 0) return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
+    return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
 }
 
 }  // namespace sinkattn

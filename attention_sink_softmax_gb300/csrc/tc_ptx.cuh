@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace sinkattn {
@@ -262,13 +263,22 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
     return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate:
-//   [4,6) D format 1 = f32; [7,10) A format 1 = bf16; [10,13) B format 1 = bf16;
-//   [15] A major (0 = K-major, 1 = MN-major); [16] B major;
+// Instruction descriptor, kind::f16 with fp32 accumulate:
+//   [4,6) D format 1 = f32; [7,10) A format (0 = f16, 1 = bf16); [10,13) B format
+//   (same); [15] A major (0 = K-major, 1 = MN-major); [16] B major;
 //   [17,23) N >> 3; [24,29) M >> 4.
+// A and B always have the same format (both bf16 or both f16).
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, int a_mn_major, int b_mn_major,
+                                                      bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) |
-           ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return idesc_kind_f16(M, N, a_mn_major, b_mn_major, false);
+}
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+    return idesc_kind_f16(M, N, a_mn_major, b_mn_major, true);
 }
 
 // Packed pairs of fp32 in one 64-bit register and the sm_100-family paired
@@ -305,6 +315,30 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// In-place conversion of `bytes` bytes of bf16 values in shared memory to f16,
+// by the 32 lanes of one warp (`bytes` a multiple of 512). Element positions
+// are kept, so a swizzled MMA operand stays a valid operand of the same shape.
+// A bf16 value converts exactly when its magnitude is within f16's range (up to
+// 65504; below 2^-17 the f16 subnormal spacing of 2^-24 rounds it); larger
+// magnitudes become infinite. The caller fences for the async proxy.
+__device__ __forceinline__ void bf16_to_f16_inplace(uint8_t* base, uint32_t bytes, int lane) {
+    uint4* p = reinterpret_cast<uint4*>(base);
+    const uint32_t n = bytes / 16;
+    auto cvt = [](uint32_t w) {
+        return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    };
+#pragma unroll 4
+    for (uint32_t i = lane; i < n; i += 32) {
+        const uint4 x = p[i];
+        p[i] = make_uint4(cvt(x.x), cvt(x.y), cvt(x.z), cvt(x.w));
+    }
 }
 
 }  // namespace tc

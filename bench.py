@@ -1,8 +1,9 @@
 """Benchmark: sink-attention forward + backward (incl. dS_h) on GB300.
 
-One step = one pass of the whole hot path over one batch: sink_attn_fwd, then
-sink_attn_bwd_preprocess (delta and dS_h) and sink_attn_bwd_main (dQ, dK, dV),
-all through the C ABI. The default workload is the GPT-OSS-20B-shaped
+One step = one pass of the whole hot path over one batch: sink_attn_fwd_ex
+(O, o_lo and LSE), then sink_attn_bwd_preprocess_ex (delta from o + o_lo, and
+dS_h) and sink_attn_bwd_main (dQ, dK, dV), all through the C ABI: the path
+whose outputs the parity tests hold to the stated tolerance. The default workload is the GPT-OSS-20B-shaped
 full-causal layer (B=2, N=8192, H_q=64, H_kv=8, d=64, bf16). Its inputs (302 MB
 of Q/K/V/dO) exceed the 129 MB L2, so no extra flush is done between steps.
 
@@ -21,19 +22,27 @@ cores, bounded sample).
 Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
 instead (the only reference this method has), on a bounded sample.
 ``--decode`` prints a separate line for the decode path (KV-cache bandwidth).
+
+``--gpus N`` without a launcher starts N processes itself, one per GPU (it
+fails with a clear message if fewer GPUs are visible); under torchrun the
+launcher's ranks are used.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import datetime
 import hashlib
 import json
 import math
 import os
+import platform
+import socket
 import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import torch
@@ -73,17 +82,18 @@ def flops_of(w, window):
 
 def bytes_of(w) -> dict:
     """Algorithmic bytes per step (each tensor read or written once):
-    forward reads Q, K, V and writes O and LSE; the preprocess reads O, dO and
-    LSE and writes D; the backward main reads Q, K, V, dO, LSE and D and writes
-    dQ, dK and dV. The fp32 dQ accumulator is implementation traffic, not
-    counted."""
+    forward reads Q, K, V and writes O, o_lo (bf16) and LSE; the preprocess
+    reads O, o_lo, dO and LSE and writes D; the backward main reads Q, K, V,
+    dO, LSE and D and writes dQ, dK and dV. The fp32 dQ accumulator is
+    implementation traffic, not counted."""
     T = w.total_tokens
     e = 2 if w.dtype == torch.bfloat16 else 4
     q = T * w.h_q * w.head_dim * e   # Q, O, dO, dQ each
     kv = T * w.h_kv * w.head_dim * e  # K, V, dK, dV each
     row = 4 * w.h_q * T               # LSE or D (fp32)
-    return {"fwd": q + 2 * kv + q + row,
-            "bwd_preprocess": 2 * q + row + row,
+    lo = q if w.dtype == torch.bfloat16 else 0  # o_lo: written by the forward, read by the preprocess
+    return {"fwd": q + 2 * kv + q + lo + row,
+            "bwd_preprocess": 2 * q + lo + row + row,
             "bwd_main": q + 2 * kv + q + 2 * row + q + 2 * kv}
 
 
@@ -177,6 +187,116 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+class NvmlClockSampler:
+    """Read-only NVML samples (SM clock, max SM clock, power, clock-event
+    reasons) every ``period_s`` from a thread, between mark_start and
+    mark_end, so that a timed region of a few tens of milliseconds still gets
+    samples. Calls libnvidia-ml through ctypes; ``ok`` is False if it cannot
+    be loaded or the device not found (then ClockSampler's nvidia-smi samples
+    are used)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self._run = threading.Event()
+        self._thread = None
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            except Exception:
+                uuid = None
+            rc = -1
+            if uuid:
+                name = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                rc = self.nv.nvmlDeviceGetHandleByUUID(name.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h))
+            self.ok = rc == 0
+        except OSError:
+            self.ok = False
+
+    def _sample(self):
+        sm, smax, mw, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(sm)) != 0:
+            return None
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(smax))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(reasons))
+        return (sm.value, smax.value, mw.value / 1000.0, reasons.value)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            if self._run.is_set():
+                x = self._sample()
+                if x is not None:
+                    self.samples.append(x)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        return self
+
+    def mark_start(self):
+        self._run.set()
+
+    def mark_end(self):
+        self._run.clear()
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        names = sorted({n for s in self.samples for bit, n in self.REASONS.items() if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": names,
+                "samples": len(self.samples), "power_w_max": max(s[2] for s in self.samples),
+                "source": f"NVML every {self.period * 1000:.0f} ms inside the timed region"}
+
+
+class Clocks:
+    """NVML samples when available, else nvidia-smi's (ClockSampler)."""
+
+    def __init__(self, device_index: int):
+        self.nvml = NvmlClockSampler(device_index)
+        self.smi = None if self.nvml.ok else ClockSampler(device_index)
+
+    def __enter__(self):
+        (self.nvml if self.smi is None else self.smi).__enter__()
+        return self
+
+    def mark_start(self):
+        (self.nvml if self.smi is None else self.smi).mark_start()
+
+    def mark_end(self):
+        (self.nvml if self.smi is None else self.smi).mark_end()
+
+    def __exit__(self, *exc):
+        (self.nvml if self.smi is None else self.smi).__exit__(*exc)
+
+    def summary(self):
+        if self.smi is None:
+            got = self.nvml.summary()
+            if got is not None:
+                return got
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no NVML sample"], "samples": 0}
+        return self.smi.summary()
+
+
 # ----------------------------------------------------------------------------- distributed
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -216,6 +336,34 @@ def config_of(w: inputs.Workload, window: int, ws: int) -> dict:
             "window": window, "tokens": w.total_tokens,
             "flops_per_step": sum(flops_of(w, window)), "l2": "inputs exceed L2 (no flush)",
             "parallelism": f"replicas x{ws} (independent batches, no collective)"}
+
+
+def spawn_ranks(n: int, argv, extra_env=None) -> int:
+    """Runs ``argv`` as n ranks of one job on this node (RANK, LOCAL_RANK,
+    WORLD_SIZE, MASTER_ADDR=127.0.0.1, a free MASTER_PORT), each a fresh
+    process; rank 0's output passes through, the others' is discarded unless
+    they fail. Returns the largest exit code."""
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ)
+        env.update({"RANK": str(r), "LOCAL_RANK": str(r), "WORLD_SIZE": str(n),
+                    "LOCAL_WORLD_SIZE": str(n), "MASTER_ADDR": "127.0.0.1",
+                    "MASTER_PORT": str(port)})
+        env.update(extra_env or {})
+        out = None if r == 0 else subprocess.PIPE
+        procs.append(subprocess.Popen(list(argv), env=env, stdout=out, stderr=out))
+    rc = 0
+    for r, p in enumerate(procs):
+        o, e = p.communicate()
+        if p.returncode != 0 and r != 0:
+            sys.stderr.write(f"rank {r} exited {p.returncode}\n")
+            if e:
+                sys.stderr.write(e.decode(errors="replace")[-4000:])
+        rc = max(rc, p.returncode)
+    return rc
 
 
 def barrier(ws):
@@ -275,6 +423,52 @@ def profiled_traffic(kernel_source, stage):
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the machine)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return platform.machine()
+
+
+def oracle_single_core_config0() -> dict:
+    """The oracle's fp64 forward + backward of workload 0 (the whole problem) on
+    one host core: a fresh interpreter with OMP_NUM_THREADS=1."""
+    code = ("import sys, time, json; sys.path.insert(0, %r)\n"
+            "import oracle\nfrom attention_sink_softmax_gb300 import inputs\n"
+            "w = inputs.workload(0); p = inputs.make_inputs(w)\n"
+            "kw = dict(scale=1 / 8, causal=True, window=0)\n"
+            "best = 1e9\n"
+            "for _ in range(5):\n"
+            "    t = time.perf_counter()\n"
+            "    oracle.forward(p['q'], p['k'], p['v'], p['sinks'], **kw)\n"
+            "    oracle.backward(p['q'], p['k'], p['v'], p['sinks'], p['dout'], **kw)\n"
+            "    best = min(best, time.perf_counter() - t)\n"
+            "print(json.dumps({'seconds': best, 'threads': oracle.num_threads()}))\n") % ROOT
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                             env=env, timeout=300)
+        d = json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal
+        return {"error": f"{type(e).__name__}"}
+    w = inputs.workload(0)
+    f = sum(flops_of(w, w.window))
+    return {"seconds": d["seconds"], "cores": d["threads"], "tflops": f / d["seconds"] / 1e12,
+            "workload": w.name, "note": "best of 5, whole problem, fp64 forward + backward"}
+
+
 def time_oracle(w, prob, window, budget_s=20.0, heads=None):
     """fp64 oracle fwd+bwd on a bounded sample: batch/sequence 0, the query heads
     of key/value head 0 (or ``heads`` of them), all rows. Returns a dict."""
@@ -319,21 +513,24 @@ def run_reference(args, w, window):
         flops = info["flops"]
     ms = 1000 * sum(times) / len(times)
     value = flops / (ms / 1000) / 1e12
+    full = sum(flops_of(w, window))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(w, window, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": info["cores"],
-                         "kind": "oracle", "sample": info["sample"]},
+                         "kind": "oracle", "sample": info["sample"], "cpu_model": cpu_model(),
+                         "sample_fraction_of_step": flops / full,
+                         "ms_per_full_step_at_this_rate": ms * full / flops},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     emit(line, rank)
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, lse, dq, dk, dv,
-            dsinks, work, flops_step):
+def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse, dq, dk,
+            dv, dsinks, work, flops_step):
     """Same step through the public API with pinned host buffers: every step's
     inputs are copied in and every output copied back inside the timed region,
     as a training loop runs it: the next step's inputs are copied in on one
@@ -343,6 +540,8 @@ def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, ls
     import attention_sink_softmax_gb300 as sa
     host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
     outs0 = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dsinks": dsinks}
+    if o_lo is not None:
+        outs0["o_lo"] = o_lo
     host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs0.items()}
     ins0 = {"q": q, "k": k, "v": v, "sinks": sinks, "dout": dout}
     dev_in = [ins0, {n: torch.empty_like(t) for n, t in ins0.items()}]
@@ -366,11 +565,20 @@ def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, ls
         stream.wait_event(in_ready[b])
         if used[b]:
             stream.wait_event(out_done[b])  # step i-2's outputs have been copied out
-        sa.sink_attn_fwd(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
-                         lse=dout_["lse"], workspace=work, params=p, stream=stream)
-        sa.sink_attn_bwd(din["q"], din["k"], din["v"], din["sinks"], dout_["o"], dout_["lse"],
-                         din["dout"], cu, dq=dout_["dq"], dk=dout_["dk"], dv=dout_["dv"],
-                         dsinks=dout_["dsinks"], workspace=work, params=p, stream=stream)
+        if "o_lo" in dout_:
+            sa.sink_attn_fwd_ex(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
+                                o_lo=dout_["o_lo"], lse=dout_["lse"], workspace=work, params=p,
+                                stream=stream)
+            sa.sink_attn_bwd_ex(din["q"], din["k"], din["v"], din["sinks"], dout_["o"],
+                                dout_["o_lo"], dout_["lse"], din["dout"], cu, dq=dout_["dq"],
+                                dk=dout_["dk"], dv=dout_["dv"], dsinks=dout_["dsinks"],
+                                workspace=work, params=p, stream=stream)
+        else:
+            sa.sink_attn_fwd(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
+                             lse=dout_["lse"], workspace=work, params=p, stream=stream)
+            sa.sink_attn_bwd(din["q"], din["k"], din["v"], din["sinks"], dout_["o"], dout_["lse"],
+                             din["dout"], cu, dq=dout_["dq"], dk=dout_["dk"], dv=dout_["dv"],
+                             dsinks=dout_["dsinks"], workspace=work, params=p, stream=stream)
         comp_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -416,6 +624,7 @@ def run_gpu(args, w, window):
     p = sa.make_params(q, k, cu, max_seqlen=w.seqlen, causal=w.causal, window=window,
                        softmax_scale=w.scale)
     o = torch.empty_like(q)
+    o_lo = torch.empty_like(q) if q.dtype == torch.bfloat16 else None
     lse = torch.empty(p.h_q, p.total_tokens, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dsinks = torch.empty_like(sinks)
@@ -426,11 +635,19 @@ def run_gpu(args, w, window):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
+        if o_lo is not None:
+            sa.sink_attn_fwd_ex(q, k, v, sinks, cu, out=o, o_lo=o_lo, lse=lse, workspace=work,
+                                params=p)
+        else:
+            sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
         if ev is not None:
             ev[1].record(stream)
-        sa.sink_attn_bwd_preprocess(p, sinks, o, lse, dout, delta=delta, dsinks=dsinks,
-                                    workspace=work)
+        if o_lo is not None:
+            sa.sink_attn_bwd_preprocess_ex(p, sinks, o, o_lo, lse, dout, delta=delta,
+                                           dsinks=dsinks, workspace=work)
+        else:
+            sa.sink_attn_bwd_preprocess(p, sinks, o, lse, dout, delta=delta, dsinks=dsinks,
+                                        workspace=work)
         if ev is not None:
             ev[2].record(stream)
         sa.sink_attn_bwd_main(p, q, k, v, lse, delta, dout, cu, dq=dq, dk=dk, dv=dv,
@@ -450,7 +667,7 @@ def run_gpu(args, w, window):
     launches0 = sa.sink_attn_kernel_launches()
     torch.cuda.synchronize(dev)
     barrier(ws)
-    with ClockSampler(local) as clk:
+    with Clocks(local) as clk:
         torch.cuda.synchronize(dev)
         clk.mark_start()
         start.record(stream)
@@ -475,8 +692,8 @@ def run_gpu(args, w, window):
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, lse, dq,
-                      dk, dv, dsinks, work, flops_step)
+        e2e = run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse,
+                      dq, dk, dv, dsinks, work, flops_step)
 
     pk, pk_src = peaks()
     # per-stage rates: FLOP/s (backward also without the S recompute, 8 d per
@@ -499,12 +716,16 @@ def run_gpu(args, w, window):
     # (their traffic entry is the sum of one launch of each)
     stage = "bwd_main" if w.head_dim == 64 else "bwd_main_d128"
     traffic = profiled_traffic(kernel_sources(stage), stage) if stage in KERNEL_SOURCES else None
-    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    # The step lasts milliseconds and draws far below the power cap, so the
+    # denominator is the burst bf16 peak (a GEMM timed alone); the sustained
+    # figure (seconds-long loop under the power cap) is given beside it.
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if f_bwd / nbytes["bwd_main"] >= ridge:
         roofline = {"bound": "tensor", "achieved": main_tflops,
-                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
-                    "kernel": "sink_attn_bwd_main", "peak_kind": f"bf16 sustained ({pk_src})"}
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": main_tflops / pk["bf16_tflops"], "traffic": traffic,
+                    "kernel": "sink_attn_bwd_main", "peak_kind": f"bf16 burst ({pk_src})",
+                    "frac_of_sustained": main_tflops / pk["bf16_tflops_sustained"]}
     else:
         main_gbs = stage_rates["bwd_main"]["gb_per_s"]
         roofline = {"bound": "hbm", "achieved": main_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -520,7 +741,7 @@ def run_gpu(args, w, window):
         "config": config_of(w, window, ws),
         "pct_of_peak": {"burst": 100 * value / ws / pk["bf16_tflops"],
                         "sustained": 100 * value / ws / pk["bf16_tflops_sustained"],
-                        "source": pk_src},
+                        "source": pk_src, "headline": "burst"},
         "stages_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1], "bwd_main": stage_ms[2]},
         "stage_rates": stage_rates,
         "clocks": clk.summary(),
@@ -532,7 +753,8 @@ def run_gpu(args, w, window):
         info = time_oracle(w, prob_host, window)
         line["cpu_baseline"] = {"value": info["value"], "unit": "TFLOP/s", "cores": info["cores"],
                                 "kind": "oracle", "sample": info["sample"],
-                                "seconds": info["seconds"]}
+                                "seconds": info["seconds"], "cpu_model": cpu_model(),
+                                "single_core_config0": oracle_single_core_config0()}
     emit(line, rank)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -640,6 +862,13 @@ def main():
     args = ap.parse_args()
     w = inputs.workload(args.config)
     window = w.window if args.window is None else args.window
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # no launcher: one process per GPU, started here
+        if args.impl == "gb300" or args.decode:
+            have = torch.cuda.device_count()
+            if have < args.gpus:
+                sys.exit(f"bench.py --gpus {args.gpus}: only {have} GPU(s) visible")
+        sys.exit(spawn_ranks(args.gpus, [sys.executable, os.path.abspath(__file__)] + sys.argv[1:]))
     if args.decode:
         run_decode(args)
     elif args.impl == "reference":

@@ -46,10 +46,35 @@
  *
  * Errors. Every entry point returns a status. Arguments are validated before
  * anything is enqueued; an invalid call enqueues nothing. A failed launch is
- * reported as SINK_ERR_CUDA. Conditions found on the device (a wait that gave
- * up, a sequence longer than max_seqlen) set a flag word at the start of the
- * workspace; sink_attn_fetch_device_error reads and clears it. Nothing is
- * thrown across the ABI.
+ * reported as SINK_ERR_CUDA. Conditions found on the device set a flag word at
+ * the start of the workspace; sink_attn_fetch_device_error reads and clears
+ * it. Its bits:
+ *   SINK_FLAG_TIMEOUT      a bounded wait inside a kernel gave up (the wait
+ *                          limit is sink_attn_set_wait_limit_ns); the outputs
+ *                          of that call are invalid;
+ *   SINK_FLAG_SEQ_TOO_LONG a sequence is longer than max_seqlen: its rows past
+ *                          max_seqlen were not computed;
+ *   SINK_FLAG_BAD_SEQLENS  cu_seqlens is not a valid packing: some
+ *                          cu_seqlens[s] < 0, cu_seqlens[s+1] < cu_seqlens[s],
+ *                          cu_seqlens[s+1] > total_tokens, or cu_seqlens[0]
+ *                          != 0. cu_seqlens lives in device memory, so this is
+ *                          checked by the kernels: every kernel checks the
+ *                          bounds of its sequence before any load or store and
+ *                          skips a sequence that fails (its outputs are left
+ *                          as they were, except dq on the bf16 64-wide path,
+ *                          which is written as 0 there). Other sequences are
+ *                          computed.
+ * Nothing is thrown across the ABI.
+ *
+ * Precision of D. The backward forms D_i = dout_i . O_i from the forward's
+ * output. The plain entry points (sink_attn_fwd / sink_attn_bwd) use the
+ * stored O, which carries its own rounding to the output dtype; with bf16 and
+ * sharp attention (dP_ij close to D_i) that rounding reaches dq, dk and dsinks
+ * through dS = P (dP - D). The _ex entry points take an extra buffer o_lo
+ * (same shape and dtype as o, bf16 only): the forward writes into it what the
+ * rounding of O to bf16 dropped, bf16(O - bf16(O)), and the backward forms
+ * D from o + o_lo, about 16 bits of O. Training code keeps o_lo with o and lse
+ * between the forward and the backward.
  */
 #ifndef SINK_ATTN_H
 #define SINK_ATTN_H
@@ -66,6 +91,11 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* Bits of the device flag word (see Errors above). */
+#define SINK_FLAG_TIMEOUT 1u
+#define SINK_FLAG_SEQ_TOO_LONG 2u
+#define SINK_FLAG_BAD_SEQLENS 4u
 
 typedef struct CUstream_st* sink_stream_t; /* same object as cudaStream_t; NULL = legacy default stream */
 
@@ -109,6 +139,16 @@ SINK_API sink_status_t sink_attn_fwd(const sink_attn_params_t* params,
                             void* o, float* lse,
                             void* workspace, size_t workspace_bytes, sink_stream_t stream);
 
+/* Forward as sink_attn_fwd, and, when o_lo is not NULL (bf16 params only;
+ * NULL is required for fp32), o_lo [same shape as o] receives
+ * bf16(O - bf16(O)) per element, the part of O that the bf16 output dropped
+ * (see "Precision of D" above). o and lse are identical to sink_attn_fwd's. */
+SINK_API sink_status_t sink_attn_fwd_ex(const sink_attn_params_t* params,
+                               const void* q, const void* k, const void* v,
+                               const float* sinks, const int32_t* cu_seqlens,
+                               void* o, void* o_lo, float* lse,
+                               void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
 /* Full backward (section "反向传播的实现"): given the forward's o and lse and the
  * upstream gradient dout, writes dq (input dtype), dk, dv (input dtype, summed
  * over the query heads of each key/value head) and dsinks (fp32 [h_q],
@@ -126,6 +166,17 @@ SINK_API sink_status_t sink_attn_bwd(const sink_attn_params_t* params,
                             void* dq, void* dk, void* dv, float* dsinks,
                             void* workspace, size_t workspace_bytes, sink_stream_t stream);
 
+/* Full backward as sink_attn_bwd, with D formed from o + o_lo (o_lo from
+ * sink_attn_fwd_ex; NULL gives exactly sink_attn_bwd). dv does not depend on
+ * D and equals sink_attn_bwd's. Equivalent to sink_attn_bwd_preprocess_ex
+ * into workspace followed by sink_attn_bwd_main. */
+SINK_API sink_status_t sink_attn_bwd_ex(const sink_attn_params_t* params,
+                               const void* q, const void* k, const void* v,
+                               const float* sinks, const int32_t* cu_seqlens,
+                               const void* o, const void* o_lo, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, float* dsinks,
+                               void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
 /* Backward step 1 (section "反向传播的实现", simplified equation): writes
  * delta[h, t] = dout_t,h . o_t,h (fp32 [h_q, T]) and
  * dsinks[h] = -sum_t exp(S_h - lse[h, t]) * delta[h, t]. Memory-bound. */
@@ -135,8 +186,20 @@ SINK_API sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params
                                        void* workspace, size_t workspace_bytes,
                                        sink_stream_t stream);
 
-/* Backward step 2: recomputes P = exp(S - lse) and writes dq, dk, dv, using
- * delta from step 1. dS_ij = P_ij (dout_i . v_j - delta_i). */
+/* Backward step 1 as above, with delta[h, t] = dout_t,h . (o_t,h + o_lo_t,h)
+ * when o_lo is not NULL (bf16 only). */
+SINK_API sink_status_t sink_attn_bwd_preprocess_ex(const sink_attn_params_t* params,
+                                          const float* sinks, const void* o, const void* o_lo,
+                                          const float* lse, const void* dout, float* delta,
+                                          float* dsinks, void* workspace, size_t workspace_bytes,
+                                          sink_stream_t stream);
+
+/* Backward step 2 (section "反向传播的实现": the gradients of the scores and
+ * through them of Q, K and V; the sink's own gradient is step 1's): recomputes
+ * P = exp(S - lse), which needs no sink term because lse includes the sink,
+ * and writes dq, dk, dv using delta from step 1:
+ * dS_ij = P_ij (dout_i . v_j - delta_i), dq = scale dS K, dk = scale dS^T Q,
+ * dv = P^T dout. */
 SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
                                  const void* q, const void* k, const void* v,
                                  const int32_t* cu_seqlens, const float* lse,
@@ -146,10 +209,10 @@ SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
 
 /* Reads and clears the device flag word at the start of a workspace that was
  * passed to the calls above. SYNCHRONISES the stream (it copies 4 bytes back).
- * Returns SINK_OK, SINK_ERR_TIMEOUT (a bounded wait gave up: outputs of that
- * call are invalid), SINK_ERR_DEVICE (a sequence exceeded max_seqlen: rows past
- * it were not computed) or SINK_ERR_CUDA. *flags_out (may be NULL) receives the
- * raw flag bits. */
+ * Returns SINK_OK, SINK_ERR_TIMEOUT (SINK_FLAG_TIMEOUT is set: outputs of that
+ * call are invalid), SINK_ERR_DEVICE (another SINK_FLAG_* bit is set: a
+ * sequence exceeded max_seqlen, or cu_seqlens is not a valid packing) or
+ * SINK_ERR_CUDA. *flags_out (may be NULL) receives the raw flag bits. */
 SINK_API sink_status_t sink_attn_fetch_device_error(void* workspace, size_t workspace_bytes,
                                            sink_stream_t stream, uint32_t* flags_out);
 
@@ -215,6 +278,14 @@ SINK_API sink_status_t sink_attn_decode(const sink_attn_params_t* params,
 
 /* Static description of a status code. Never NULL. */
 SINK_API const char* sink_attn_status_str(sink_status_t status);
+
+/* Every wait inside the tensor-core kernels (on a copy or a product another
+ * warp issued) gives up after a time limit, raises SINK_FLAG_TIMEOUT and lets
+ * the kernel wind down, instead of hanging the GPU. Sets that limit for calls
+ * made after this one, in nanoseconds, process-wide; 0 restores the default
+ * (2 s). Returns the previous limit. A limit far below a kernel's normal
+ * waiting time makes correct calls fail with SINK_ERR_TIMEOUT. */
+SINK_API uint64_t sink_attn_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Number of kernels this library has enqueued in the calling process so far
  * (all entry points, all devices). Host-side counter; never synchronises. */

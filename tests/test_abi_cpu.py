@@ -32,7 +32,7 @@ def _declared_functions():
 
 def test_exports_every_declared_symbol(L):
     declared = _declared_functions()
-    assert set(_abi.EXPORTS) <= set(declared)
+    assert set(_abi.EXPORTS) | set(_abi.TESTING_EXPORTS) == set(declared)
     assert len(declared) >= 8
     for name in declared:
         assert hasattr(L, name), f"libsinkattn does not export {name}"
@@ -43,7 +43,7 @@ def test_status_strings_and_version(L):
     for st in range(7):
         assert isinstance(sa.sink_attn_status_str(st), str)
     assert sa.sink_attn_status_str(99) == "unknown status"
-    assert sa.sink_attn_version() >= 100
+    assert sa.sink_attn_version() >= 200
 
 
 def _params(**kw):
@@ -127,3 +127,20 @@ def test_decode_workspace_and_validation(L):
     assert L.sink_attn_decode(ctypes.byref(_params(causal=0)), *([nul] * 8), nul, 0, nul) == \
         _abi.SINK_ERR_INVALID_ARG
     assert L.sink_attn_decode(ctypes.byref(p), *([nul] * 8), nul, 0, nul) == _abi.SINK_ERR_WORKSPACE
+
+
+def test_wait_limit_setter_round_trip(L):
+    prev = sa.sink_attn_set_wait_limit_ns(5_000_000)
+    try:
+        assert prev == 2_000_000_000
+        assert sa.sink_attn_set_wait_limit_ns(0) == 5_000_000
+        assert sa.sink_attn_set_wait_limit_ns(0) == 2_000_000_000
+    finally:
+        sa.sink_attn_set_wait_limit_ns(0)
+
+
+def test_flag_bits_match_the_header(L):
+    text = open(os.path.join(ROOT, "include", "sink_attn.h"), encoding="utf-8").read()
+    for name in ("SINK_FLAG_TIMEOUT", "SINK_FLAG_SEQ_TOO_LONG", "SINK_FLAG_BAD_SEQLENS"):
+        m = re.search(rf"#define {name} (\d+)u", text)
+        assert m and int(m.group(1)) == getattr(_abi, name)

@@ -5,6 +5,7 @@ aggregate and the rule that rank 0 alone prints."""
 import json
 import os
 import socket
+import sys
 
 import pytest
 import torch
@@ -88,15 +89,49 @@ def test_reference_arm_line_matches_gpu_arm_config(monkeypatch, capsys):
 
 def test_algorithmic_bytes_and_flops_of_the_target_layer():
     """Per-stage algorithmic bytes and FLOPs of the causal B=2 N=8192 64/8 d=64
-    layer: forward reads Q, K, V and writes O, LSE (306 MB); the preprocess
-    reads O, dO, LSE and writes D (277 MB); 4.295e9 unmasked pairs."""
+    layer: forward reads Q, K, V and writes O, o_lo, LSE (440 MB); the
+    preprocess reads O, o_lo, dO, LSE and writes D (411 MB); 4.295e9 unmasked
+    pairs."""
     w = inputs.workload(1)
     b = bench.bytes_of(w)
-    assert b["fwd"] == 2 * 16384 * 64 * 64 * 2 + 2 * 16384 * 8 * 64 * 2 + 4 * 64 * 16384
-    assert round(b["fwd"] / 1e6) == 306 and round(b["bwd_preprocess"] / 1e6) == 277
+    assert b["fwd"] == 3 * 16384 * 64 * 64 * 2 + 2 * 16384 * 8 * 64 * 2 + 4 * 64 * 16384
+    assert round(b["fwd"] / 1e6) == 440 and round(b["bwd_preprocess"] / 1e6) == 411
     assert bench.pairs_of(w, 0) == 2 * 64 * 8192 * 8193 // 2
     f_fwd, f_bwd = bench.flops_of(w, 0)
     assert f_fwd == 4 * 64 * bench.pairs_of(w, 0) and f_bwd == 10 * 64 * bench.pairs_of(w, 0)
     # the window-128 layer's backward sits below the ridge point: HBM-bound
     w2 = inputs.workload(2)
-    assert bench.flops_of(w2, 128)[1] / bench.bytes_of(w2)["bwd_main"] < 1749.9e12 / 6796.9e9
+    assert bench.flops_of(w2, 128)[1] / bench.bytes_of(w2)["bwd_main"] < 1926.5e12 / 6688.8e9
+
+
+_RANK_SCRIPT = """
+import os, sys, json, torch
+sys.path.insert(0, {root!r})
+import bench
+ws, rank, local = bench.dist_env()
+bench.init_dist(ws, "gloo")
+ms = bench.max_over_ranks(1.0 + rank, ws, torch.device("cpu"))
+bench.emit({{"ws": ws, "rank": rank, "local": local, "ms": ms}}, rank)
+torch.distributed.destroy_process_group()
+"""
+
+
+def test_spawn_ranks_runs_one_process_per_rank(tmp_path, capfd):
+    """bench.py --gpus N without a launcher starts N processes itself
+    (spawn_ranks): here two gloo ranks of a small script; rank 0 alone prints."""
+    script = tmp_path / "rank.py"
+    script.write_text(_RANK_SCRIPT.format(root=os.path.dirname(os.path.dirname(
+        os.path.abspath(__file__)))))
+    env = {"MASTER_ADDR": "127.0.0.1"}
+    rc = bench.spawn_ranks(2, [sys.executable, str(script)], env)
+    assert rc == 0
+    lines = [l for l in capfd.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d == {"ws": 2, "rank": 0, "local": 0, "ms": 2.0}
+
+
+def test_spawn_ranks_reports_a_failing_rank(tmp_path):
+    script = tmp_path / "fail.py"
+    script.write_text("import os, sys\nsys.exit(3 if os.environ['RANK'] == '1' else 0)\n")
+    assert bench.spawn_ranks(2, [sys.executable, str(script)]) == 3
