@@ -31,7 +31,45 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
     }
 }
 
+// The backward's preparation in one pass: f16 copies of Q and K, and the fp32
+// dQ accumulator zeroed. Work items are 16-byte groups: [0, nq) of Q, then
+// [nq, nq + nk) of K, then the accumulator's groups (4 floats each).
+__global__ void __launch_bounds__(256) bwd_prepare_kernel(const uint4* __restrict__ q,
+                                                          uint4* __restrict__ q16, size_t nq,
+                                                          const uint4* __restrict__ k,
+                                                          uint4* __restrict__ k16, size_t nk,
+                                                          uint4* __restrict__ acc, size_t nacc) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t total = nq + nk + nacc;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += stride) {
+        if (i < nq) {
+            const uint4 x = __ldg(q + i);
+            q16[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                                bf16x2_to_f16x2(x.w));
+        } else if (i < nq + nk) {
+            const uint4 x = __ldg(k + (i - nq));
+            k16[i - nq] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y),
+                                     bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
+        } else {
+            acc[i - nq - nk] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t bwd_prepare(const void* q, void* q16, size_t q_elems, const void* k, void* k16,
+                        size_t k_elems, float* acc, size_t acc_floats, cudaStream_t st) {
+    const size_t nq = q_elems / 8, nk = k_elems / 8, na = acc_floats / 4;
+    const size_t total = nq + nk + na;
+    if (total == 0) return cudaSuccess;
+    const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)152 * 16);
+    bwd_prepare_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(q), static_cast<uint4*>(q16), nq,
+                                               static_cast<const uint4*>(k), static_cast<uint4*>(k16), nk,
+                                               reinterpret_cast<uint4*>(acc), na);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st) {
     const size_t n16 = elems / 8;  // callers pass whole rows of 64 or 128 elements

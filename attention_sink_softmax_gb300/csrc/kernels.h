@@ -14,6 +14,10 @@ void count_launches(unsigned n);
 // f16 copy of `elems` bf16 values (a multiple of 8; 16-byte aligned buffers),
 // exact within f16's range (convert.cu).
 cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st);
+// f16 copies of q (q_elems) and k (k_elems) and acc_floats zeros, in one pass
+// (the 64-wide tensor-core backward's preparation; convert.cu).
+cudaError_t bwd_prepare(const void* q, void* q16, size_t q_elems, const void* k, void* k16,
+                        size_t k_elems, float* acc, size_t acc_floats, cudaStream_t st);
 
 // CUDA-core path (any dtype the ABI accepts, head_dim 64).
 // o_lo (nullable, bf16 only): receives bf16(O - bf16(O)) per element.

@@ -303,29 +303,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const bool pd_ready = it == 0 || mbar_test_wait(&sm.pd_free, (it - 1) & 1);
                 const bool ds_ready = it <= 1 || mbar_test_wait(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1);
                 tmem_ld_wait();
-                if (it > 1) {
-                    ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
-                                                                        ((it >> 1) - 1) & 1, flags,
-                                                                        abort_word, P.wait_ns));
-                    if (!ok) break;
-                }
-                // dS row of this key (f16): 64 query rows = 128 bytes of atom w of the
-                // step's buffer; written before the tensor-memory stores below so that
-                // the proxy fence after them finds these stores done
-                uint8_t* atom = sm.ds[it & 1][w];
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
+                for (int j = 0; j < 64; j += 4) {
                     // dS = P (dP - delta), two columns per paired op (the MMA subtracted delta)
-                    float y[8];
-#pragma unroll
-                    for (int u = 0; u < 8; u += 2) {
-                        const int j = 8 * c16 + u;
-                        const uint64_t t = f2_pack(__uint_as_float(dv64[j]), __uint_as_float(dv64[j + 1]));
-                        f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t), y[u], y[u + 1]);
-                        pd[j / 2] = pack_f16x2(y[u], y[u + 1]);
-                    }
-                    *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) =
-                        make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
+                    const uint32_t* d = dv64 + j;
+                    const uint64_t t01 = f2_pack(__uint_as_float(d[0]), __uint_as_float(d[1]));
+                    const uint64_t t23 = f2_pack(__uint_as_float(d[2]), __uint_as_float(d[3]));
+                    float y0, y1, y2, y3;
+                    f2_unpack(f2_mul(f2_pack(p[j], p[j + 1]), t01), y0, y1);
+                    f2_unpack(f2_mul(f2_pack(p[j + 2], p[j + 3]), t23), y2, y3);
+                    pd[j / 2] = pack_f16x2(y0, y1);
+                    pd[j / 2 + 1] = pack_f16x2(y2, y3);
                 }
                 // dP^T has been read: the next step's S^T may overwrite the columns
                 tc_fence_before();
@@ -335,6 +323,21 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                                                                         abort_word, P.wait_ns));
                     if (!ok) break;
                 }
+                if (it > 1) {
+                    ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
+                                                                        ((it >> 1) - 1) & 1, flags,
+                                                                        abort_word, P.wait_ns));
+                    if (!ok) break;
+                }
+            }
+            // dS row of this key (f16): 64 query rows = 128 bytes of atom w (A operand
+            // of dQ); written before the tensor-memory stores so that the proxy fence
+            // below finds them done
+            uint8_t* atom = sm.ds[it & 1][w];
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16) {
+                const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
+                *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
@@ -595,8 +598,9 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
     // f16 copies of Q and K for the f16 products (the same 2-byte layout)
     void* q16 = static_cast<char*>(workspace) + acc_bytes(P);
     void* k16 = static_cast<char*>(q16) + q16_bytes(P);
-    cudaError_t e = convert_bf16_to_f16(q, q16, (size_t)P.total * P.h_q * kD, st);
-    if (e == cudaSuccess) e = convert_bf16_to_f16(k, k16, (size_t)P.total * P.h_kv * kD, st);
+    // ... and the fp32 dQ accumulator zeroed, in one memory-bound pass
+    const size_t n = (size_t)P.total * P.h_q * kD;
+    cudaError_t e = bwd_prepare(q, q16, n, k, k16, (size_t)P.total * P.h_kv * kD, acc, n, st);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mdo, mdq;
     if (!make_head_tile_map(&mq, q16, P.total, P.h_q, kBM) ||
@@ -611,9 +615,6 @@ cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     const size_t smem = sizeof(BwdSmem) + 1024;
     e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const size_t n = (size_t)P.total * P.h_q * kD;
-    e = cudaMemsetAsync(acc, 0, n * sizeof(float), st);
     if (e != cudaSuccess) return e;
     dim3 grid((P.max_seqlen + kBN - 1) / kBN, P.h_kv, P.nseq);
     bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k16,
