@@ -33,7 +33,8 @@ __all__ = [
     "SinkAttnParams", "SinkAttnError", "make_params", "sink_attn_workspace_bytes",
     "sink_attn_fwd", "sink_attn_bwd", "sink_attn_bwd_preprocess", "sink_attn_bwd_main",
     "sink_attn_fwd_ex", "sink_attn_bwd_ex", "sink_attn_bwd_preprocess_ex",
-    "sink_attn_set_wait_limit_ns", "sink_attn_testing_withhold_load",
+    "sink_attn_set_wait_limit_ns", "sink_attn_set_deterministic",
+    "sink_attn_testing_withhold_load",
     "sink_attn_fetch_device_error", "sink_attn_bwd_preprocess_noalloc",
     "sink_attn_noalloc_scratch_bytes", "sink_attn_status_str", "sink_attn_kernel_launches",
     "sink_attn_version", "make_decode_params", "sink_attn_decode_workspace_bytes",
@@ -407,6 +408,14 @@ def sink_attn_set_wait_limit_ns(limit_ns: int) -> int:
     """Limit of every bounded wait inside the kernels, for calls made after this
     one (process-wide); 0 restores the default of 2 s. Returns the previous limit."""
     return int(lib().sink_attn_set_wait_limit_ns(int(limit_ns)))
+
+
+def sink_attn_set_deterministic(on: bool) -> bool:
+    """Reproducible dq for backward calls made after this one (process-wide):
+    the 64-wide bf16 backward then runs as a key-owning dK/dV kernel and a
+    query-owning dQ kernel with no reduce-adds. Slower; off by default. The
+    workspace size depends on it. Returns the previous setting."""
+    return bool(lib().sink_attn_set_deterministic(1 if on else 0))
 
 
 def sink_attn_testing_withhold_load(on: bool) -> None:

@@ -45,6 +45,7 @@ EXPORTS = (
     "sink_attn_decode",
     "sink_attn_status_str",
     "sink_attn_set_wait_limit_ns",
+    "sink_attn_set_deterministic",
     "sink_attn_kernel_launches",
     "sink_attn_version",
 )
@@ -130,6 +131,8 @@ def lib():
             L.sink_attn_status_str.restype = ctypes.c_char_p
             L.sink_attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.sink_attn_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.sink_attn_set_deterministic.argtypes = [ctypes.c_int]
+            L.sink_attn_set_deterministic.restype = ctypes.c_int
             L.sink_attn_testing_withhold_load.argtypes = [ctypes.c_int]
             L.sink_attn_testing_withhold_load.restype = None
             L.sink_attn_kernel_launches.argtypes = []

@@ -28,6 +28,7 @@ static std::atomic<uint64_t> g_launches{0};
 // limit of every bounded device wait, and the test hook that withholds loads
 static std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 static std::atomic<int> g_withhold_load{0};
+static std::atomic<int> g_deterministic{0};
 
 namespace sinkattn {
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -102,6 +103,7 @@ Problem make_problem(const sink_attn_params_t* p, const int32_t* cu) {
     P.cu = cu;
     P.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     P.withhold_load = g_withhold_load.load(std::memory_order_relaxed);
+    P.deterministic = g_deterministic.load(std::memory_order_relaxed);
     return P;
 }
 
@@ -377,6 +379,10 @@ uint64_t sink_attn_kernel_launches(void) { return g_launches.load(std::memory_or
 
 uint64_t sink_attn_set_wait_limit_ns(uint64_t limit_ns) {
     return g_wait_ns.exchange(limit_ns ? limit_ns : kDefaultWaitNs, std::memory_order_relaxed);
+}
+
+int sink_attn_set_deterministic(int on) {
+    return g_deterministic.exchange(on ? 1 : 0, std::memory_order_relaxed);
 }
 
 void sink_attn_testing_withhold_load(int on) {

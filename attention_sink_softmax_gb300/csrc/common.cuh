@@ -35,6 +35,7 @@ struct Problem {
     const int32_t* cu; // device cu_seqlens or nullptr (padded: sequence s = [s*N, s*N+N))
     uint64_t wait_ns;  // limit of each bounded wait (kDefaultWaitNs unless a test lowers it)
     int withhold_load; // test hook: the forward / backward producer stops after its first stage
+    int deterministic; // backward: dQ without reduce-adds (the split 64-wide backward)
 };
 
 // Decode (one query per entry against a key/value cache), see decode.cu.

@@ -147,6 +147,10 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* a, float f) {
                       pack_bf16x2(__uint_as_float(a[6]) * f, __uint_as_float(a[7]) * f));
 }
 
+// kDq = false: the same kernel without its dQ part (no dS in shared memory, no
+// dQ product, the drain warps idle): the key-owning half of the split
+// backward, whose dQ comes from tc_bwd_dq.cu.
+template <bool kDq>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmDQ,
@@ -301,7 +305,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // this step's dS buffer by the dQ product of two steps back: poll their
                 // barriers now, while the loads are in flight, and wait below if needed
                 const bool pd_ready = it == 0 || mbar_test_wait(&sm.pd_free, (it - 1) & 1);
-                const bool ds_ready = it <= 1 || mbar_test_wait(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1);
+                const bool ds_ready = !kDq || it <= 1 || mbar_test_wait(&sm.ds_free[it & 1], ((it >> 1) - 1) & 1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 64; j += 4) {
@@ -323,7 +327,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                                                                         abort_word, P.wait_ns));
                     if (!ok) break;
                 }
-                if (it > 1) {
+                if (kDq && it > 1) {
                     ok = __all_sync(0xffffffffu, ds_ready || wait_phase(&sm.ds_free[it & 1],
                                                                         ((it >> 1) - 1) & 1, flags,
                                                                         abort_word, P.wait_ns));
@@ -333,11 +337,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // dS row of this key (f16): 64 query rows = 128 bytes of atom w (A operand
             // of dQ); written before the tensor-memory stores so that the proxy fence
             // below finds them done
-            uint8_t* atom = sm.ds[it & 1][w];
+            if (kDq) {
+                uint8_t* atom = sm.ds[it & 1][w];
 #pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16) {
-                const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
-                *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    const uint4 val = make_uint4(pd[4 * c16], pd[4 * c16 + 1], pd[4 * c16 + 2], pd[4 * c16 + 3]);
+                    *reinterpret_cast<uint4*>(atom + sw128(kr, c16 * 16)) = val;
+                }
             }
             tc_fence_after();
             tmem_st32(tmem + lane_off + kColP + 32 * w, pp);
@@ -373,6 +379,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain
         regs_decrease<kDqRegs>();
+        if (kDq) {
         const int wq = warp - 12;
         const int r = wq * 32 + lane;  // query row within the step (tensor-memory lane)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -411,6 +418,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         }
         if (issuer) bulk_wait_all<0>();
+        }  // kDq
     } else {
         regs_decrease<kCtlRegs>();
         if (warp == 8) {
@@ -538,18 +546,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // P^T, dS^T and the step's Q / dO stage are no longer read
                 mma_commit(&sm.pd_free);
                 mma_commit(&sm.q_empty[st]);
-                // dQ = dS K  (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
-                if (j > 0) {
-                    if (!(ok = wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word, P.wait_ns))) break;
-                    tc_fence_after();
-                }
+                if (kDq) {
+                    // dQ = dS K  (A = dS, MN-major: query rows contiguous, 2 atoms of 64)
+                    if (j > 0) {
+                        if (!(ok = wait_phase(&sm.dq_consumed, (j - 1) & 1, flags, abort_word, P.wait_ns))) break;
+                        tc_fence_after();
+                    }
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[j & 1][0]) + kk * 2048, kBN * 128, 1024);
-                    mma_ss(tmem + kColDQ, da, dKmn + (uint64_t)((kk * 2048) >> 4), idQ, kk > 0);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t da = smem_desc_sw128(smem_u32(sm.ds[j & 1][0]) + kk * 2048, kBN * 128, 1024);
+                        mma_ss(tmem + kColDQ, da, dKmn + (uint64_t)((kk * 2048) >> 4), idQ, kk > 0);
+                    }
+                    mma_commit(&sm.ds_free[j & 1]);
+                    mma_commit(&sm.grads_done);
                 }
-                mma_commit(&sm.ds_free[j & 1]);
-                mma_commit(&sm.grads_done);
             }
             if (ok) mma_commit(&sm.acc_done);
             mma_commit(&sm.drained[1]);
@@ -580,8 +590,18 @@ bool tc_bwd_supported(const Problem& P, bool bf16) {
     return bf16 && P.head_dim == kD && P.total > 0;
 }
 
-// [dQ accumulator fp32 [T, h_q, 64]][Q in f16 [T, h_q, 64]][K in f16 [T, h_kv, 64]]
-static size_t acc_bytes(const Problem& P) { return sizeof(float) * (size_t)P.total * P.h_q * kD; }
+// The deterministic mode (Problem::deterministic) runs the split backward: this
+// kernel without its dQ part for dK and dV, and the row-owning dQ kernel
+// (tc_bwd_dq.cu), which sums each dQ row over its key blocks in tensor memory
+// in a fixed order and writes it once, so dQ is reproducible bit for bit. It
+// recomputes S and dP for dQ and is slower than the fused kernel, whose dQ
+// blocks meet by reduce-adds in a run-dependent order.
+static bool split_bwd(const Problem& P) { return P.deterministic != 0; }
+
+// [dQ accumulator fp32 [T, h_q, 64] (fused only)][Q in f16 [T, h_q, 64]][K in f16 [T, h_kv, 64]]
+static size_t acc_bytes(const Problem& P) {
+    return split_bwd(P) ? 0 : sizeof(float) * (size_t)P.total * P.h_q * kD;
+}
 static size_t q16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_q * kD; }
 static size_t k16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_kv * kD; }
 
@@ -590,38 +610,54 @@ size_t tc_bwd_workspace_bytes(const Problem& P, bool bf16) {
     return acc_bytes(P) + q16_bytes(P) + k16_bytes(P);
 }
 
+template <bool kDq>
+static cudaError_t launch_bwd_kernel(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
+                                     const CUtensorMap& mdo, const CUtensorMap& mdq, const void* k16,
+                                     const void* v, const float* lse, const float* delta, void* dk,
+                                     void* dv, uint32_t* flags, cudaStream_t st) {
+    // the register split is only safe at exactly this launch value
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, bwd_tc_kernel<kDq>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    const size_t smem = sizeof(BwdSmem) + 1024;
+    e = cudaFuncSetAttribute(bwd_tc_kernel<kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((P.max_seqlen + kBN - 1) / kBN, P.h_kv, P.nseq);
+    bwd_tc_kernel<kDq><<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k16,
+                                                     (const __nv_bfloat16*)v, lse, delta,
+                                                     (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, flags);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v,
                    const float* lse, const float* delta, const void* dout, void* dq, void* dk,
                    void* dv, uint32_t* flags, void* workspace, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
+    const bool split = split_bwd(P);
     float* acc = static_cast<float*>(workspace);
-    // f16 copies of Q and K for the f16 products (the same 2-byte layout)
+    // f16 copies of Q and K for the f16 products (the same 2-byte layout) and, for
+    // the fused kernel, the fp32 dQ accumulator zeroed, in one memory-bound pass
     void* q16 = static_cast<char*>(workspace) + acc_bytes(P);
     void* k16 = static_cast<char*>(q16) + q16_bytes(P);
-    // ... and the fp32 dQ accumulator zeroed, in one memory-bound pass
     const size_t n = (size_t)P.total * P.h_q * kD;
-    cudaError_t e = bwd_prepare(q, q16, n, k, k16, (size_t)P.total * P.h_kv * kD, acc, n, st);
+    cudaError_t e = bwd_prepare(q, q16, n, k, k16, (size_t)P.total * P.h_kv * kD, acc,
+                                split ? 0 : n, st);
     if (e != cudaSuccess) return e;
-    CUtensorMap mq, mk, mdo, mdq;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     if (!make_head_tile_map(&mq, q16, P.total, P.h_q, kBM) ||
         !make_head_tile_map(&mk, k16, P.total, P.h_kv, kBN) ||
-        !make_head_tile_map(&mdo, dout, P.total, P.h_q, kBM) ||
-        !make_f32_head_half_map(&mdq, acc, P.total, P.h_q, kBM))
+        !make_head_tile_map(&mdo, dout, P.total, P.h_q, kBM))
         return cudaErrorInvalidValue;
-    // the register split is only safe at exactly this launch value
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_tc_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    const size_t smem = sizeof(BwdSmem) + 1024;
-    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((P.max_seqlen + kBN - 1) / kBN, P.h_kv, P.nseq);
-    bwd_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, mdo, mdq, P, (const __nv_bfloat16*)k16,
-                                                (const __nv_bfloat16*)v, lse, delta,
-                                                (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, flags);
-    count_launches(1);
-    e = cudaGetLastError();
+    if (split) {
+        if (!make_head_tile_map(&mv, v, P.total, P.h_kv, kBN)) return cudaErrorInvalidValue;
+        e = launch_bwd_kernel<false>(P, mq, mk, mdo, mdo, k16, v, lse, delta, dk, dv, flags, st);
+        if (e != cudaSuccess) return e;
+        return tc_bwd_dq64(P, mk, mv, q16, dout, lse, delta, dq, flags, st);
+    }
+    if (!make_f32_head_half_map(&mdq, acc, P.total, P.h_q, kBM)) return cudaErrorInvalidValue;
+    e = launch_bwd_kernel<true>(P, mq, mk, mdo, mdq, k16, v, lse, delta, dk, dv, flags, st);
     if (e != cudaSuccess) return e;
     const size_t n4 = n / 4;
     const int blocks = (int)std::min<size_t>((n4 + 255) / 256, 152 * 32);

@@ -156,9 +156,9 @@ SINK_API sink_status_t sink_attn_fwd_ex(const sink_attn_params_t* params,
  * order so it is bitwise reproducible). dk, dv and dsinks are bitwise
  * reproducible; dq on the bf16 d = 64 path is summed over key blocks by fp32
  * reduce-adds into the workspace in an order that varies between runs, so it
- * may differ in the last bf16 place (at d = 128 and in fp32 it is
- * reproducible). Equivalent to sink_attn_bwd_preprocess into workspace
- * followed by sink_attn_bwd_main. */
+ * may differ in the last bf16 place, unless sink_attn_set_deterministic is on
+ * (at d = 128 and in fp32 it is reproducible either way). Equivalent to
+ * sink_attn_bwd_preprocess into workspace followed by sink_attn_bwd_main. */
 SINK_API sink_status_t sink_attn_bwd(const sink_attn_params_t* params,
                             const void* q, const void* k, const void* v,
                             const float* sinks, const int32_t* cu_seqlens,
@@ -286,6 +286,18 @@ SINK_API const char* sink_attn_status_str(sink_status_t status);
  * (2 s). Returns the previous limit. A limit far below a kernel's normal
  * waiting time makes correct calls fail with SINK_ERR_TIMEOUT. */
 SINK_API uint64_t sink_attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Reproducible dq (process-wide, for calls made after this one; returns the
+ * previous setting). Off (0, the default): the bf16 64-wide backward sums dq
+ * over key blocks by fp32 reduce-adds whose order varies between runs, so dq
+ * may differ in the last bf16 place from run to run (dk, dv and dsinks are
+ * always reproducible). On (1): that backward runs as two kernels instead, a
+ * key-owning one for dk and dv and a query-owning one that sums each dq row in
+ * a fixed order and writes it once, so dq is reproducible bit for bit; it
+ * recomputes the scores for dq and takes about 1.45x as long. The workspace
+ * size (sink_attn_workspace_bytes) depends on this setting. Other paths are
+ * reproducible either way. */
+SINK_API int sink_attn_set_deterministic(int on);
 
 /* Number of kernels this library has enqueued in the calling process so far
  * (all entry points, all devices). Host-side counter; never synchronises. */

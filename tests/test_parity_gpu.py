@@ -175,6 +175,29 @@ def test_o_lo_is_the_rounding_residual_of_o():
     assert np.all(np.abs(lo64) <= 2.0 ** -8 * np.abs(o64) + 1e-30)
 
 
+@pytest.mark.parametrize("window", [0, 128])
+def test_deterministic_mode_gives_reproducible_dq(window):
+    """sink_attn_set_deterministic(1): the 64-wide backward as a dK/dV kernel
+    and a query-owning dQ kernel. dq is then the same bit for bit on every run
+    and within tolerance of the oracle (large logits included); dk, dv and
+    dS_h equal the default path's bit for bit (the same kernels compute them)."""
+    for gain in (1.0, 4.0):
+        prob = inputs.random_problem(15, [700, 300], 8, 2, 64, dtype=torch.bfloat16, packed=True,
+                                     sink_scale=2.0, qk_gain=gain)
+        default = _run(prob, window=window, scale=0.125)
+        prev = sa.sink_attn_set_deterministic(True)
+        try:
+            runs = [_run(prob, window=window, scale=0.125) for _ in range(3)]
+        finally:
+            sa.sink_attn_set_deterministic(prev)
+        for r in runs[1:]:
+            for x, y in zip(r, runs[0]):
+                assert torch.equal(x, y)
+        for i in (0, 1, 3, 4, 5):  # O, LSE, dK, dV, dS_h
+            assert torch.equal(runs[0][i], default[i]), i
+        _check(prob, torch.bfloat16, window=window, scale=0.125, got=runs[0])
+
+
 def test_empty_input():
     q = torch.empty(0, 4, 64, dtype=torch.bfloat16, device=DEV)
     k = torch.empty(0, 1, 64, dtype=torch.bfloat16, device=DEV)
