@@ -167,6 +167,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int seq = blockIdx.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
+    if (L > P.max_seqlen) {
+        // as in the forward: rows and keys past max_seqlen are not computed
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
+        L = P.max_seqlen;
+    }
     const int k0 = kb * kBN;
     if (k0 >= L) return;  // uniform for the CTA, before any barrier or TMEM use
 

@@ -70,6 +70,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int h = blockIdx.y, seq = blockIdx.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
+    if (L > P.max_seqlen) {
+        // as in the forward: rows and keys past max_seqlen are not computed
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
+        L = P.max_seqlen;
+    }
     const int r0 = rb * kB;
     if (r0 >= L) return;  // uniform for the CTA, before any barrier or tensor memory
     int kb_lo = 0, kb_hi = (L - 1) / kB;

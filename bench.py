@@ -31,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import datetime
 import hashlib
 import json
@@ -855,12 +856,20 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=1, help="workload index 0..5")
     ap.add_argument("--window", type=int, default=None, help="override the workload's window")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (padded workloads only): a smaller "
+                         "case of the same layer, e.g. for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode path (KV-cache bandwidth) instead of the training step")
     args = ap.parse_args()
     w = inputs.workload(args.config)
+    if args.batch is not None:
+        if w.packed or args.batch < 1:
+            sys.exit("--batch takes a positive batch for a padded workload")
+        w = dataclasses.replace(w, batch=args.batch,
+                                name=w.name.replace(f"_B{w.batch}_", f"_B{args.batch}_"))
     window = w.window if args.window is None else args.window
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         # no launcher: one process per GPU, started here

@@ -52,17 +52,20 @@
  *   SINK_FLAG_TIMEOUT      a bounded wait inside a kernel gave up (the wait
  *                          limit is sink_attn_set_wait_limit_ns); the outputs
  *                          of that call are invalid;
- *   SINK_FLAG_SEQ_TOO_LONG a sequence is longer than max_seqlen: its rows past
- *                          max_seqlen were not computed;
+ *   SINK_FLAG_SEQ_TOO_LONG a sequence is longer than max_seqlen: its rows and
+ *                          keys past max_seqlen were not computed (their
+ *                          outputs are left as they were, except dq on the
+ *                          default bf16 64-wide path, written as 0);
  *   SINK_FLAG_BAD_SEQLENS  cu_seqlens is not a valid packing: some
  *                          cu_seqlens[s] < 0, cu_seqlens[s+1] < cu_seqlens[s],
  *                          cu_seqlens[s+1] > total_tokens, or cu_seqlens[0]
  *                          != 0. cu_seqlens lives in device memory, so this is
  *                          checked by the kernels: every kernel checks the
  *                          bounds of its sequence before any load or store and
- *                          skips a sequence that fails (its outputs are left
- *                          as they were, except dq on the bf16 64-wide path,
- *                          which is written as 0 there). Other sequences are
+ *                          skips a sequence that fails (its rows of o and lse
+ *                          and its keys' dk and dv are left as they were; its
+ *                          rows of dq too, except on the default bf16 64-wide
+ *                          path, which writes 0 there). Other sequences are
  *                          computed.
  * Nothing is thrown across the ABI.
  *
