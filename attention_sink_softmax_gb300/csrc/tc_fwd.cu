@@ -893,6 +893,14 @@ size_t tc_fwd_workspace_bytes(const Problem& P, bool bf16) {
     return bf16 ? (size_t)P.total * P.h_kv * P.head_dim * 2 : 0;
 }
 
+// True if the compiled kernel uses exactly the register count its setmaxnreg
+// split was sized for.
+template <typename Kernel>
+static bool launch_regs_ok(Kernel kernel) {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.numRegs == kLaunchRegs;
+}
+
 template <int NT, int D>
 static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const float* sinks, void* o, void* o_lo,
@@ -952,11 +960,17 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
         !make_head_tile_map(&mv, v16, P.total, P.h_kv, kBN, P.head_dim))
         return cudaErrorInvalidValue;
     if (P.head_dim == 128) return launch_fwd<1, 128>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
+    // The two-tile kernels split their registers (setmaxnreg) and run only if
+    // the compiler gave them exactly kLaunchRegs; otherwise the one-tile kernel
+    // of the same kind (no split) computes the same result.
+    const bool pair = P.group % 2 == 0;
     if (P.causal && P.window > 0 && P.window <= 2 * kBN) {
-        if (P.group % 2 == 0) return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
+        if (pair && launch_regs_ok(fwd_tc_tiles_kernel<2>))
+            return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
         return launch_fwd_tiles<1>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     }
-    if (P.group % 2 == 0) return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
+    if (pair && launch_regs_ok(fwd_tc_kernel<2, 64>))
+        return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
 }
 

@@ -403,23 +403,25 @@ def kernel_sources(stage):
     return [os.path.join(csrc, f) for f in KERNEL_SOURCES[stage]]
 
 
-def profiled_traffic(kernel_source, stage):
-    """DRAM traffic per launch from the committed ncu summary, if the kernel's
-    source is unchanged since it was captured; else None."""
+def profiled_traffic(kernel_source, stage, workload):
+    """DRAM traffic per launch of a stage's kernel(s) on a workload, from the
+    committed ncu summary, if the kernel's source is unchanged since it was
+    captured; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
     digest = source_digest(kernel_source)
     with open(path, encoding="utf-8") as f:
         for line in f:
-            if line.startswith("| ") and f"| {stage} |" in line:
-                cells = [c.strip() for c in line.strip().strip("|").split("|")]
-                # | stage | source digest | bytes per launch | ...
-                if len(cells) >= 3 and cells[1] == digest:
-                    try:
-                        return float(cells[2])
-                    except ValueError:
-                        return None
+            if not line.startswith("| "):
+                continue
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            # | stage | workload | source digest | bytes per launch | ...
+            if len(cells) >= 4 and cells[0] == stage and cells[1] == workload and cells[2] == digest:
+                try:
+                    return float(cells[3])
+                except ValueError:
+                    return None
     return None
 
 
@@ -716,7 +718,8 @@ def run_gpu(args, w, window):
     # the 64-wide backward is one kernel; at d = 128 it is the dQ and dK/dV kernels
     # (their traffic entry is the sum of one launch of each)
     stage = "bwd_main" if w.head_dim == 64 else "bwd_main_d128"
-    traffic = profiled_traffic(kernel_sources(stage), stage) if stage in KERNEL_SOURCES else None
+    traffic = (profiled_traffic(kernel_sources(stage), stage, w.name) if stage in KERNEL_SOURCES
+               else None)
     # The step lasts milliseconds and draws far below the power cap, so the
     # denominator is the burst bf16 peak (a GEMM timed alone); the sustained
     # figure (seconds-long loop under the power cap) is given beside it.
@@ -841,7 +844,8 @@ def run_decode(args):
                    "l2": "KV cache exceeds L2 (no flush)", "launch": launch},
         "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "traffic": profiled_traffic(kernel_sources("decode"), "decode"),
+                     "frac": gbs / pk["hbm_gbs"],
+                     "traffic": profiled_traffic(kernel_sources("decode"), "decode", w.name),
                      "kernel": "decode_mma_kernel",
                      "peak_kind": f"HBM copy ({pk_src})"},
     }
