@@ -75,6 +75,26 @@ __device__ __forceinline__ bool seq_bounds_checked(const Problem& P, int s, int&
     return true;
 }
 
+// This block's (x, y, z) for a grid of (row or key blocks, heads, sequences),
+// read from the linear launch index with z (the sequence) slowest, then x,
+// then y (the head) fastest. Blocks are dispatched roughly in linear-index
+// order with x fastest; under a causal mask a block's work depends on its x,
+// and with x fastest every (head, sequence) slice ran long-to-short in turn,
+// so the last slice's longest blocks started late and most SMs idled while
+// they finished. With the heads innermost, the blocks of one sequence run
+// longest-first across all heads, and one sequence's Q / dO stay the working
+// set in L2 (an order with x slowest over all sequences spread the working set
+// over every packed sequence at once).
+struct BlockCoord {
+    int x, y, z;
+};
+__device__ __forceinline__ BlockCoord block_seq_x_head() {
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const unsigned xy = gridDim.x * gridDim.y;
+    const unsigned r = lin % xy;
+    return BlockCoord{(int)(r / gridDim.y), (int)(r % gridDim.y), (int)(lin / xy)};
+}
+
 // First allowed key of row i.
 __device__ __forceinline__ int key_lo(const Problem& P, int i) {
     if (!P.causal) return 0;

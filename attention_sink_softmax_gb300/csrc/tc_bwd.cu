@@ -162,14 +162,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kb = blockIdx.x;  // key block; block 0 sees the most rows under a causal mask
-    const int hk = blockIdx.y;
-    const int seq = blockIdx.z;
+    const BlockCoord bc = block_seq_x_head();
+    const int kb = bc.x;  // key block; block 0 sees the most rows under a causal mask
+    const int hk = bc.y;
+    const int seq = bc.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     if (L > P.max_seqlen) {
         // as in the forward: rows and keys past max_seqlen are not computed
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
+        if (kb == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
         L = P.max_seqlen;
     }
     const int k0 = kb * kBN;

@@ -94,8 +94,9 @@ bwd128_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int rb = gridDim.x - 1 - blockIdx.x;  // longest row blocks first
-    const int h = blockIdx.y, seq = blockIdx.z;
+    const BlockCoord bc = block_seq_x_head();
+    const int rb = gridDim.x - 1 - bc.x;  // longest row blocks first
+    const int h = bc.y, seq = bc.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     const int r0 = rb * kB;
@@ -382,7 +383,8 @@ bwd128_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     DkvSmem& sm = *reinterpret_cast<DkvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kb = blockIdx.x, hk = blockIdx.y, seq = blockIdx.z;
+    const BlockCoord bc = block_seq_x_head();  // key block 0 (the longest) first
+    const int kb = bc.x, hk = bc.y, seq = bc.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     const int j0 = kb * kB;

@@ -66,13 +66,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int rb = gridDim.x - 1 - blockIdx.x;  // longest row blocks first
-    const int h = blockIdx.y, seq = blockIdx.z;
+    const BlockCoord bc = block_seq_x_head();
+    const int rb = gridDim.x - 1 - bc.x;  // longest row blocks first
+    const int h = bc.y, seq = bc.z;
     int start, L;
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     if (L > P.max_seqlen) {
         // as in the forward: rows and keys past max_seqlen are not computed
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
+        if (bc.x == 0 && threadIdx.x == 0) atomicOr(flags, kFlagSeqTooLong);
         L = P.max_seqlen;
     }
     const int r0 = rb * kB;
