@@ -10,10 +10,14 @@
 namespace sinkattn {
 
 // Backward step 1: delta = rowsum(dO * O) in [h_q, T] and per-chunk partials of
-// sum_t exp(S_h - LSE_t) * delta_t. One block = one head x kPreTokens tokens;
-// kD / 8 lanes share one row, each lane one 16-byte (bf16) or 32-byte (fp32)
-// piece of 8 elements. A thread issues the loads of 8 of its rows before using
-// any, so every thread keeps 8 rows of O and dO in flight (memory-bound step).
+// sum_t exp(S_h - LSE_t) * delta_t. One block = one head x kPreTokens tokens
+// (a chunk); kD / 8 lanes share one row, each lane one 16-byte (bf16) or
+// 32-byte (fp32) piece of 8 elements. A thread issues the loads of 8 of its
+// rows before using any, so every thread keeps 8 rows of O and dO in flight
+// (memory-bound step). The head is the grid's x, so the blocks that run at
+// the same time read every head of a few consecutive chunks: whole [token,
+// head, d] rows of memory, not one head's 128-byte piece out of every
+// h_q * 128 bytes. Chunks past the grid's y (more than 65535) loop.
 constexpr int kPreTokens = 256;
 constexpr int kPreThreads = 256;
 
@@ -72,53 +76,57 @@ preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restri
     constexpr int kBatch = 8;  // rows of a thread in flight at once
     static_assert(kIters % kBatch == 0, "row batches");
     __shared__ float warp_sum[kPreThreads / 32];
-    const int h = blockIdx.y;
-    const int t0 = blockIdx.x * kPreTokens;
+    const int h = blockIdx.x;
+    const int nchunks = (total + kPreTokens - 1) / kPreTokens;
     const int sub = threadIdx.x % kLanes;
     const int r0 = threadIdx.x / kLanes;
     const float sink = __ldg(sinks + h);
-    float mine = 0.f;  // this row-group's running sum, added in token order
-    for (int b0 = 0; b0 < kIters; b0 += kBatch) {
-        Piece8<T> po[kBatch], pd[kBatch], pl[kLo ? kBatch : 1];
-        float lz[kBatch];
+    for (int chunk = blockIdx.y; chunk < nchunks; chunk += gridDim.y) {
+        const int t0 = chunk * kPreTokens;
+        float mine = 0.f;  // this row-group's running sum, added in token order
+        for (int b0 = 0; b0 < kIters; b0 += kBatch) {
+            Piece8<T> po[kBatch], pd[kBatch], pl[kLo ? kBatch : 1];
+            float lz[kBatch];
 #pragma unroll
-        for (int x = 0; x < kBatch; ++x) {
-            const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
-            if (t < total) {
-                const size_t off = ((size_t)t * h_q + h) * kD + sub * kPer;
-                po[x] = load_piece(o + off);
-                pd[x] = load_piece(dout + off);
-                if (kLo) pl[kLo ? x : 0] = load_piece(o_lo + off);
-                lz[x] = __ldg(lse + (size_t)h * total + t);
+            for (int x = 0; x < kBatch; ++x) {
+                const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
+                if (t < total) {
+                    const size_t off = ((size_t)t * h_q + h) * kD + sub * kPer;
+                    po[x] = load_piece(o + off);
+                    pd[x] = load_piece(dout + off);
+                    if (kLo) pl[kLo ? x : 0] = load_piece(o_lo + off);
+                    lz[x] = __ldg(lse + (size_t)h * total + t);
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < kBatch; ++x) {
+                const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
+                float dsum = 0.f;
+                if (t < total) {
+                    // dO . o_lo first: the smaller term, added before the main one
+                    dsum = kLo ? dot_piece(pl[kLo ? x : 0], pd[x]) : 0.f;
+                    dsum += dot_piece(po[x], pd[x]);
+                }
+#pragma unroll
+                for (int w = kLanes / 2; w >= 1; w >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, w);
+                if (t < total) {
+                    if (sub == 0) delta[(size_t)h * total + t] = dsum;
+                    mine += expf(sink - lz[x]) * dsum;
+                }
             }
         }
+        // fixed-order reduction: the first lane of each row group, then warps in order
+        if (sub != 0) mine = 0.f;
 #pragma unroll
-        for (int x = 0; x < kBatch; ++x) {
-            const int t = t0 + r0 + (b0 + x) * kRowsPerIter;
-            float dsum = 0.f;
-            if (t < total) {
-                // dO . o_lo first: the smaller term, added before the main one
-                dsum = kLo ? dot_piece(pl[kLo ? x : 0], pd[x]) : 0.f;
-                dsum += dot_piece(po[x], pd[x]);
-            }
-#pragma unroll
-            for (int w = kLanes / 2; w >= 1; w >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, w);
-            if (t < total) {
-                if (sub == 0) delta[(size_t)h * total + t] = dsum;
-                mine += expf(sink - lz[x]) * dsum;
-            }
+        for (int w = 16; w >= 1; w >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, w);
+        if (threadIdx.x % 32 == 0) warp_sum[threadIdx.x / 32] = mine;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float acc = 0.f;
+            for (int w = 0; w < kPreThreads / 32; ++w) acc += warp_sum[w];
+            partial[(size_t)h * nchunks + chunk] = acc;
         }
-    }
-    // fixed-order reduction: the first lane of each row group, then warps in order
-    if (sub != 0) mine = 0.f;
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, w);
-    if (threadIdx.x % 32 == 0) warp_sum[threadIdx.x / 32] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float acc = 0.f;
-        for (int w = 0; w < kPreThreads / 32; ++w) acc += warp_sum[w];
-        partial[(size_t)h * gridDim.x + blockIdx.x] = acc;
+        __syncthreads();  // warp_sum is rewritten by the next chunk
     }
 }
 
@@ -152,7 +160,7 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
                            float* dsinks, float* partial, cudaStream_t st) {
     const int nchunks = preprocess_chunks(P.total);
     if (nchunks > 0) {
-        dim3 grid(nchunks, P.h_q);
+        dim3 grid(P.h_q, nchunks < 65535 ? nchunks : 65535);
         const bool d128 = P.head_dim == 128;
         if (bf16 && d128)
             launch_preprocess<__nv_bfloat16, 128>(grid, st, P, o, o_lo, dout, lse, sinks, delta, partial);
