@@ -32,6 +32,7 @@ from ._abi import SinkAttnError, SinkAttnParams, lib, status_str  # noqa: F401
 __all__ = [
     "SinkAttnParams", "SinkAttnError", "make_params", "sink_attn_workspace_bytes",
     "sink_attn_fwd", "sink_attn_bwd", "sink_attn_bwd_preprocess", "sink_attn_bwd_main",
+    "sink_attn_bwd_prepare",
     "sink_attn_fwd_ex", "sink_attn_bwd_ex", "sink_attn_bwd_preprocess_ex",
     "sink_attn_set_wait_limit_ns", "sink_attn_set_deterministic",
     "sink_attn_testing_withhold_load",
@@ -275,22 +276,42 @@ def sink_attn_bwd_preprocess_ex(params, sinks, o, o_lo, lse, dout, *, delta=None
 
 
 def sink_attn_bwd_main(params, q, k, v, lse, delta, dout, cu_seqlens=None, *, dq=None, dk=None,
-                       dv=None, workspace=None, stream=None):
-    """Backward step 2: returns (dq, dk, dv)."""
+                       dv=None, workspace=None, stream=None, prepared=False):
+    """Backward step 2: returns (dq, dk, dv). prepared=True (sink_attn_bwd_main_ex
+    with SINK_BWD_PREPARED) skips the preparation pass, which
+    sink_attn_bwd_prepare must already have run on the same workspace."""
     _check_qkv(q, k, v)
     _need_cuda("dout", dout, q.dtype)
     _need_cuda("lse", lse, torch.float32)
     _need_cuda("delta", delta, torch.float32)
+    if prepared and workspace is None:
+        raise ValueError("prepared=True needs the workspace sink_attn_bwd_prepare filled")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     workspace = _workspace(params, True, q.device, workspace)
-    st = lib().sink_attn_bwd_main(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v),
-                                  _ptr(cu_seqlens), _ptr(lse), _ptr(delta), _ptr(dout), _ptr(dq),
-                                  _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-                                  _stream(stream, q.device))
-    _abi.check(st, "sink_attn_bwd_main")
+    st = lib().sink_attn_bwd_main_ex(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(cu_seqlens), _ptr(lse), _ptr(delta), _ptr(dout),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                     workspace.numel(),
+                                     _abi.SINK_BWD_PREPARED if prepared else 0,
+                                     _stream(stream, q.device))
+    _abi.check(st, "sink_attn_bwd_main_ex")
     return dq, dk, dv
+
+
+def sink_attn_bwd_prepare(params, q, k, *, workspace, stream=None):
+    """The backward's preparation pass on its own (f16 copies of q and k, the
+    zeroed dQ accumulator, into `workspace`); it depends on q and k alone, so
+    it can run on a second stream while the forward runs. Follow it with
+    sink_attn_bwd_main(..., workspace=workspace, prepared=True), ordered after
+    it (an event). Returns the workspace."""
+    _check_qkv(q, k, k)
+    workspace = _workspace(params, True, q.device, workspace)
+    st = lib().sink_attn_bwd_prepare(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(workspace),
+                                     workspace.numel(), _stream(stream, q.device))
+    _abi.check(st, "sink_attn_bwd_prepare")
+    return workspace
 
 
 def sink_attn_bwd_preprocess_noalloc(params, sinks, o, lse, dout, *, delta=None, dsinks=None,

@@ -28,6 +28,8 @@ SINK_FLAG_TIMEOUT = 1
 SINK_FLAG_SEQ_TOO_LONG = 2
 SINK_FLAG_BAD_SEQLENS = 4
 
+SINK_BWD_PREPARED = 1  # options bit of sink_attn_bwd_main_ex
+
 # names declared in include/sink_attn.h, in declaration order
 EXPORTS = (
     "sink_attn_workspace_bytes",
@@ -38,6 +40,8 @@ EXPORTS = (
     "sink_attn_bwd_preprocess",
     "sink_attn_bwd_preprocess_ex",
     "sink_attn_bwd_main",
+    "sink_attn_bwd_prepare",
+    "sink_attn_bwd_main_ex",
     "sink_attn_fetch_device_error",
     "sink_attn_bwd_preprocess_noalloc",
     "sink_attn_noalloc_scratch_bytes",
@@ -116,6 +120,10 @@ def lib():
             L.sink_attn_bwd_preprocess_ex.restype = ctypes.c_int
             L.sink_attn_bwd_main.argtypes = [_PP] + [_P] * 10 + [_P, ctypes.c_size_t, _P]
             L.sink_attn_bwd_main.restype = ctypes.c_int
+            L.sink_attn_bwd_prepare.argtypes = [_PP, _P, _P, _P, ctypes.c_size_t, _P]
+            L.sink_attn_bwd_prepare.restype = ctypes.c_int
+            L.sink_attn_bwd_main_ex.argtypes = ([_PP] + [_P] * 10 + [_P, ctypes.c_size_t, ctypes.c_uint, _P])
+            L.sink_attn_bwd_main_ex.restype = ctypes.c_int
             L.sink_attn_fetch_device_error.argtypes = [_P, ctypes.c_size_t, _P,
                                                        ctypes.POINTER(ctypes.c_uint32)]
             L.sink_attn_fetch_device_error.restype = ctypes.c_int

@@ -218,11 +218,38 @@ sink_status_t sink_attn_bwd_preprocess(const sink_attn_params_t* params, const f
                                        workspace, workspace_bytes, stream);
 }
 
+sink_status_t sink_attn_bwd_prepare(const sink_attn_params_t* params, const void* q,
+                                    const void* k, void* workspace, size_t workspace_bytes,
+                                    sink_stream_t stream) {
+    sink_status_t st = validate(params);
+    if (st != SINK_OK) return st;
+    // the pass covers all total_tokens rows and needs no sequence layout
+    if (!workspace || !aligned16(workspace) || !device_accessible(workspace)) return SINK_ERR_WORKSPACE;
+    const BwdLayout L = bwd_layout(params);
+    if (workspace_bytes < L.total) return SINK_ERR_WORKSPACE;
+    if (!empty(params) && !all_aligned({q, k})) return SINK_ERR_INVALID_ARG;
+    if (empty(params)) return SINK_OK;
+    const Problem P = make_problem(params, nullptr);
+    const bool bf16 = params->dtype == SINK_BF16;
+    if (!tc_bwd_supported(P, bf16)) return SINK_OK;  // only the 64-wide tensor-core path prepares
+    return cuda_status(tc_bwd_prepare(P, q, k, (char*)workspace + L.tc, (cudaStream_t)stream));
+}
+
 sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params, const void* q, const void* k,
                                  const void* v, const int32_t* cu_seqlens, const float* lse,
                                  const float* delta, const void* dout, void* dq, void* dk,
                                  void* dv, void* workspace, size_t workspace_bytes,
                                  sink_stream_t stream) {
+    return sink_attn_bwd_main_ex(params, q, k, v, cu_seqlens, lse, delta, dout, dq, dk, dv,
+                                 workspace, workspace_bytes, 0u, stream);
+}
+
+sink_status_t sink_attn_bwd_main_ex(const sink_attn_params_t* params, const void* q,
+                                    const void* k, const void* v, const int32_t* cu_seqlens,
+                                    const float* lse, const float* delta, const void* dout,
+                                    void* dq, void* dk, void* dv, void* workspace,
+                                    size_t workspace_bytes, unsigned options, sink_stream_t stream) {
+    if (options & ~SINK_BWD_PREPARED) return SINK_ERR_INVALID_ARG;
     sink_status_t st = validate(params);
     if (st != SINK_OK) return st;
     if ((st = validate_layout(params, cu_seqlens)) != SINK_OK) return st;
@@ -238,7 +265,7 @@ sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params, const void* q
     cudaError_t e;
     if (tc_bwd_supported(P, bf16))
         e = tc_bwd(P, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace,
-                   (char*)workspace + L.tc, s);
+                   (char*)workspace + L.tc, (options & SINK_BWD_PREPARED) != 0, s);
     else if (tc_bwd128_supported(P, bf16))
         e = tc_bwd128(P, q, k, v, lse, delta, dout, dq, dk, dv, (uint32_t*)workspace, s);
     else

@@ -33,15 +33,24 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
 
 // The backward's preparation in one pass: f16 copies of Q and K, and the fp32
 // dQ accumulator zeroed. Work items are 16-byte groups: [0, nq) of Q, then
-// [nq, nq + nk) of K, then the accumulator's groups (4 floats each).
+// [nq, nq + nk) of K, then the accumulator's groups (4 floats each). Each
+// block takes kPrepItems consecutive items and exits (no grid-stride loop):
+// run on a low-priority stream beside the forward, short blocks hand their SM
+// back to the forward's CTAs as soon as those are ready to run.
+constexpr int kPrepPerThread = 8;
+constexpr int kPrepItems = 256 * kPrepPerThread;
+
 __global__ void __launch_bounds__(256) bwd_prepare_kernel(const uint4* __restrict__ q,
                                                           uint4* __restrict__ q16, size_t nq,
                                                           const uint4* __restrict__ k,
                                                           uint4* __restrict__ k16, size_t nk,
                                                           uint4* __restrict__ acc, size_t nacc) {
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
     const size_t total = nq + nk + nacc;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += stride) {
+    const size_t base = (size_t)blockIdx.x * kPrepItems + threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < kPrepPerThread; ++j) {
+        const size_t i = base + (size_t)j * 256;
+        if (i >= total) break;
         if (i < nq) {
             const uint4 x = __ldg(q + i);
             q16[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
@@ -63,8 +72,9 @@ cudaError_t bwd_prepare(const void* q, void* q16, size_t q_elems, const void* k,
     const size_t nq = q_elems / 8, nk = k_elems / 8, na = acc_floats / 4;
     const size_t total = nq + nk + na;
     if (total == 0) return cudaSuccess;
-    const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)152 * 16);
-    bwd_prepare_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(q), static_cast<uint4*>(q16), nq,
+    const size_t blocks = (total + kPrepItems - 1) / kPrepItems;
+    if (blocks > 0x7fffffffu) return cudaErrorInvalidValue;
+    bwd_prepare_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(q), static_cast<uint4*>(q16), nq,
                                                static_cast<const uint4*>(k), static_cast<uint4*>(k16), nk,
                                                reinterpret_cast<uint4*>(acc), na);
     count_launches(1);

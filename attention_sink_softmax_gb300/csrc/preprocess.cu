@@ -12,8 +12,8 @@ namespace sinkattn {
 // Backward step 1: delta = rowsum(dO * O) in [h_q, T] and per-chunk partials of
 // sum_t exp(S_h - LSE_t) * delta_t. One block = one head x kPreTokens tokens
 // (a chunk); kD / 8 lanes share one row, each lane one 16-byte (bf16) or
-// 32-byte (fp32) piece of 8 elements. A thread issues the loads of 8 of its
-// rows before using any, so every thread keeps 8 rows of O and dO in flight
+// 32-byte (fp32) piece of 8 elements. A thread issues the loads of 4 of its
+// rows before using any, so every thread keeps 4 rows of O and dO in flight
 // (memory-bound step). The head is the grid's x, so the blocks that run at
 // the same time read every head of a few consecutive chunks: whole [token,
 // head, d] rows of memory, not one head's 128-byte piece out of every
@@ -64,7 +64,7 @@ __device__ __forceinline__ float dot_piece(const Piece8<float>& a, const Piece8<
 // delta is formed as dO . (o + o_lo), so D does not inherit the rounding of
 // the stored O.
 template <typename T, int kD, bool kLo>
-__global__ void __launch_bounds__(kPreThreads)
+__global__ void __launch_bounds__(kPreThreads, sizeof(T) == 2 ? 3 : 1)
 preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restrict__ o_lo,
                   const T* __restrict__ dout, const float* __restrict__ lse,
                   const float* __restrict__ sinks, float* __restrict__ delta,
@@ -73,7 +73,7 @@ preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restri
     constexpr int kPer = 8;
     constexpr int kRowsPerIter = kPreThreads / kLanes;
     constexpr int kIters = kPreTokens / kRowsPerIter;
-    constexpr int kBatch = 8;  // rows of a thread in flight at once
+    constexpr int kBatch = 4;  // rows of a thread in flight at once (3 blocks per SM for bf16)
     static_assert(kIters % kBatch == 0, "row batches");
     __shared__ float warp_sum[kPreThreads / 32];
     const int h = blockIdx.x;

@@ -18,9 +18,13 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
 
 bool tc_bwd_supported(const Problem& P, bool bf16);
 size_t tc_bwd_workspace_bytes(const Problem& P, bool bf16);
+// The backward's inputs-only pass (f16 copies of Q and K, the fp32 dQ
+// accumulator zeroed) into its workspace; tc_bwd skips it when `prepared`.
+cudaError_t tc_bwd_prepare(const Problem& P, const void* q, const void* k, void* workspace,
+                           cudaStream_t st);
 cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v,
                    const float* lse, const float* delta, const void* dout, void* dq, void* dk,
-                   void* dv, uint32_t* flags, void* workspace, cudaStream_t st);
+                   void* dv, uint32_t* flags, void* workspace, bool prepared, cudaStream_t st);
 
 // The row-owning dQ kernel of the split 64-wide backward (tc_bwd_dq.cu): K as
 // its f16 copy, V in bf16, Q's f16 copy; writes dq once, in bf16.

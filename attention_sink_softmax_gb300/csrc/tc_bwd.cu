@@ -605,9 +605,11 @@ bool tc_bwd_supported(const Problem& P, bool bf16) {
 static bool split_bwd(const Problem& P) { return P.deterministic != 0; }
 
 // [dQ accumulator fp32 [T, h_q, 64] (fused only)][Q in f16 [T, h_q, 64]][K in f16 [T, h_kv, 64]]
-static size_t acc_bytes(const Problem& P) {
-    return split_bwd(P) ? 0 : sizeof(float) * (size_t)P.total * P.h_q * kD;
-}
+// The accumulator's region is reserved in both backward modes (the split one
+// does not add into it), so the workspace layout does not depend on the
+// reproducible-dQ setting: a workspace prepared under one setting is laid out
+// as the main call under the other expects.
+static size_t acc_bytes(const Problem& P) { return sizeof(float) * (size_t)P.total * P.h_q * kD; }
 static size_t q16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_q * kD; }
 static size_t k16_bytes(const Problem& P) { return 2 * (size_t)P.total * P.h_kv * kD; }
 
@@ -637,20 +639,45 @@ static cudaError_t launch_bwd_kernel(const Problem& P, const CUtensorMap& mq, co
     return cudaGetLastError();
 }
 
+// Workspace of the 64-wide backward: [fp32 dQ accumulator][Q in f16][K in f16].
+static void bwd_regions(const Problem& P, void* workspace, float*& acc, void*& q16, void*& k16) {
+    acc = static_cast<float*>(workspace);
+    q16 = static_cast<char*>(workspace) + acc_bytes(P);
+    k16 = static_cast<char*>(q16) + q16_bytes(P);
+}
+
+// f16 copies of Q and K for the f16 products (the same 2-byte layout) and the
+// fp32 dQ accumulator zeroed (only the fused kernel adds into it: zero_acc),
+// in one memory-bound pass
+static cudaError_t prepare_pass(const Problem& P, const void* q, const void* k, void* workspace,
+                                bool zero_acc, cudaStream_t st) {
+    float* acc;
+    void *q16, *k16;
+    bwd_regions(P, workspace, acc, q16, k16);
+    const size_t n = (size_t)P.total * P.h_q * kD;
+    return bwd_prepare(q, q16, n, k, k16, (size_t)P.total * P.h_kv * kD, acc, zero_acc ? n : 0, st);
+}
+
+// The pass on its own (sink_attn_bwd_prepare): the accumulator is zeroed
+// whatever the reproducible-dQ setting, so the setting may change before the
+// main call without leaving it dirty.
+cudaError_t tc_bwd_prepare(const Problem& P, const void* q, const void* k, void* workspace,
+                           cudaStream_t st) {
+    if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
+    return prepare_pass(P, q, k, workspace, true, st);
+}
+
 cudaError_t tc_bwd(const Problem& P, const void* q, const void* k, const void* v,
                    const float* lse, const float* delta, const void* dout, void* dq, void* dk,
-                   void* dv, uint32_t* flags, void* workspace, cudaStream_t st) {
+                   void* dv, uint32_t* flags, void* workspace, bool prepared, cudaStream_t st) {
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
     const bool split = split_bwd(P);
-    float* acc = static_cast<float*>(workspace);
-    // f16 copies of Q and K for the f16 products (the same 2-byte layout) and, for
-    // the fused kernel, the fp32 dQ accumulator zeroed, in one memory-bound pass
-    void* q16 = static_cast<char*>(workspace) + acc_bytes(P);
-    void* k16 = static_cast<char*>(q16) + q16_bytes(P);
+    float* acc;
+    void *q16, *k16;
+    bwd_regions(P, workspace, acc, q16, k16);
     const size_t n = (size_t)P.total * P.h_q * kD;
-    cudaError_t e = bwd_prepare(q, q16, n, k, k16, (size_t)P.total * P.h_kv * kD, acc,
-                                split ? 0 : n, st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!prepared && (e = prepare_pass(P, q, k, workspace, !split, st)) != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mdo, mdq;
     if (!make_head_tile_map(&mq, q16, P.total, P.h_q, kBM) ||
         !make_head_tile_map(&mk, k16, P.total, P.h_kv, kBN) ||

@@ -3,7 +3,12 @@
 One step = one pass of the whole hot path over one batch: sink_attn_fwd_ex
 (O, o_lo and LSE), then sink_attn_bwd_preprocess_ex (delta from o + o_lo, and
 dS_h) and sink_attn_bwd_main (dQ, dK, dV), all through the C ABI: the path
-whose outputs the parity tests hold to the stated tolerance. The default workload is the GPT-OSS-20B-shaped
+whose outputs the parity tests hold to the stated tolerance. The backward's
+preparation pass (f16 copies of Q and K, the zeroed dQ accumulator), which
+depends on Q and K alone, is issued with sink_attn_bwd_prepare on a
+lower-priority stream right after the forward is queued, and
+sink_attn_bwd_main runs with SINK_BWD_PREPARED once it is done (an event);
+``--serial-prepare`` keeps it inside sink_attn_bwd_main on the one stream. The default workload is the GPT-OSS-20B-shaped
 full-causal layer (B=2, N=8192, H_q=64, H_kv=8, d=64, bf16). Its inputs (302 MB
 of Q/K/V/dO) exceed the 129 MB L2, so no extra flush is done between steps.
 
@@ -532,8 +537,8 @@ def run_reference(args, w, window):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse, dq, dk,
-            dv, dsinks, work, flops_step):
+def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse, dq,
+            dk, dv, dsinks, delta, work, flops_step):
     """Same step through the public API with pinned host buffers: every step's
     inputs are copied in and every output copied back inside the timed region,
     as a training loop runs it: the next step's inputs are copied in on one
@@ -555,6 +560,8 @@ def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
+    bwd_done = ev()
+    bwd_done.record(stream)
 
     def e2e_step(i):
         b = i % 2
@@ -572,10 +579,28 @@ def run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_
             sa.sink_attn_fwd_ex(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
                                 o_lo=dout_["o_lo"], lse=dout_["lse"], workspace=work, params=p,
                                 stream=stream)
-            sa.sink_attn_bwd_ex(din["q"], din["k"], din["v"], din["sinks"], dout_["o"],
-                                dout_["o_lo"], dout_["lse"], din["dout"], cu, dq=dout_["dq"],
-                                dk=dout_["dk"], dv=dout_["dv"], dsinks=dout_["dsinks"],
-                                workspace=work, params=p, stream=stream)
+            if args.serial_prepare:
+                sa.sink_attn_bwd_ex(din["q"], din["k"], din["v"], din["sinks"], dout_["o"],
+                                    dout_["o_lo"], dout_["lse"], din["dout"], cu, dq=dout_["dq"],
+                                    dk=dout_["dk"], dv=dout_["dv"], dsinks=dout_["dsinks"],
+                                    workspace=work, params=p, stream=stream)
+            else:
+                # the preparation beside the forward (q, k copied in; the last
+                # backward, the workspace's previous user, done)
+                side.wait_event(in_ready[b])
+                side.wait_event(bwd_done)
+                sa.sink_attn_bwd_prepare(p, din["q"], din["k"], workspace=work, stream=side)
+                prepared = ev()
+                prepared.record(side)
+                sa.sink_attn_bwd_preprocess_ex(p, din["sinks"], dout_["o"], dout_["o_lo"],
+                                               dout_["lse"], din["dout"], delta=delta,
+                                               dsinks=dout_["dsinks"], workspace=work,
+                                               stream=stream)
+                stream.wait_event(prepared)
+                sa.sink_attn_bwd_main(p, din["q"], din["k"], din["v"], dout_["lse"], delta,
+                                      din["dout"], cu, dq=dout_["dq"], dk=dout_["dk"],
+                                      dv=dout_["dv"], workspace=work, stream=stream, prepared=True)
+                bwd_done.record(stream)
         else:
             sa.sink_attn_fwd(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
                              lse=dout_["lse"], workspace=work, params=p, stream=stream)
@@ -619,7 +644,10 @@ def run_gpu(args, w, window):
     init_dist(ws, "nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
+    # the step's stream outranks the one the backward preparation runs on, so
+    # the preparation's blocks only take SMs the forward leaves idle
+    stream = torch.cuda.Stream(dev, priority=-1)
+    side = torch.cuda.Stream(dev, priority=0)
 
     prob_host = inputs.make_inputs(w, seed=rank_seed(w, rank))
     d = {k: (v.to(dev) if v is not None else None) for k, v in prob_host.items()}
@@ -635,28 +663,43 @@ def run_gpu(args, w, window):
     wsz = max(sa.sink_attn_workspace_bytes(p, False), sa.sink_attn_workspace_bytes(p, True))
     work = torch.empty(wsz, dtype=torch.uint8, device=dev)
 
+    bwd_done = torch.cuda.Event()
+    bwd_done.record(stream)
+    overlap = not args.serial_prepare
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         if o_lo is not None:
             sa.sink_attn_fwd_ex(q, k, v, sinks, cu, out=o, o_lo=o_lo, lse=lse, workspace=work,
-                                params=p)
+                                params=p, stream=stream)
         else:
-            sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p)
+            sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p,
+                             stream=stream)
+        if overlap:
+            # q and k are the step's inputs; the workspace's last user is the
+            # previous step's backward
+            side.wait_event(bwd_done)
+            sa.sink_attn_bwd_prepare(p, q, k, workspace=work, stream=side)
+            prepared = torch.cuda.Event()
+            prepared.record(side)
         if ev is not None:
             ev[1].record(stream)
         if o_lo is not None:
             sa.sink_attn_bwd_preprocess_ex(p, sinks, o, o_lo, lse, dout, delta=delta,
-                                           dsinks=dsinks, workspace=work)
+                                           dsinks=dsinks, workspace=work, stream=stream)
         else:
             sa.sink_attn_bwd_preprocess(p, sinks, o, lse, dout, delta=delta, dsinks=dsinks,
-                                        workspace=work)
+                                        workspace=work, stream=stream)
         if ev is not None:
             ev[2].record(stream)
+        if overlap:
+            stream.wait_event(prepared)
         sa.sink_attn_bwd_main(p, q, k, v, lse, delta, dout, cu, dq=dq, dk=dk, dv=dv,
-                              workspace=work)
+                              workspace=work, stream=stream, prepared=overlap)
         if ev is not None:
             ev[3].record(stream)
+        bwd_done.record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -695,8 +738,8 @@ def run_gpu(args, w, window):
     # ---- end to end through the public API with host buffers (pinned)
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, ws, dev, stream, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse,
-                      dq, dk, dv, dsinks, work, flops_step)
+        e2e = run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo,
+                      lse, dq, dk, dv, dsinks, delta, work, flops_step)
 
     pk, pk_src = peaks()
     # per-stage rates: FLOP/s (backward also without the S recompute, 8 d per
@@ -747,6 +790,9 @@ def run_gpu(args, w, window):
                         "sustained": 100 * value / ws / pk["bf16_tflops_sustained"],
                         "source": pk_src, "headline": "burst"},
         "stages_ms": {"fwd": stage_ms[0], "bwd_preprocess": stage_ms[1], "bwd_main": stage_ms[2]},
+        "bwd_prepare": ("inside sink_attn_bwd_main" if args.serial_prepare or w.head_dim != 64
+                        or w.dtype != torch.bfloat16 else
+                        "sink_attn_bwd_prepare on a lower-priority stream beside the forward"),
         "stage_rates": stage_rates,
         "clocks": clk.summary(),
         "e2e": e2e,
@@ -865,6 +911,9 @@ def main():
                          "case of the same layer, e.g. for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--serial-prepare", action="store_true",
+                    help="run the backward preparation inside sink_attn_bwd_main on the step's "
+                         "stream instead of beside the forward on a lower-priority one")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode path (KV-cache bandwidth) instead of the training step")
     args = ap.parse_args()

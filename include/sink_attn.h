@@ -210,6 +210,38 @@ SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
                                  void* dq, void* dk, void* dv,
                                  void* workspace, size_t workspace_bytes, sink_stream_t stream);
 
+/* Backward step 2 split in two, so that its memory-bound preparation can run
+ * early. The preparation depends on q and k alone: on the bf16 d = 64 path it
+ * writes f16 copies of q and k into the workspace and zeroes the fp32 dQ
+ * accumulator there (the fused backward's reduce-adds land in it); on every
+ * other path it does nothing. A caller that has q and k before the forward's
+ * outputs exist can issue sink_attn_bwd_prepare on a second, lower-priority
+ * stream while the forward runs (its blocks then take the SMs the forward's
+ * last wave leaves idle), and later sink_attn_bwd_main_ex with
+ * SINK_BWD_PREPARED, which skips the pass.
+ * The caller orders the two calls (an event), passes both the same params,
+ * q, k and workspace (sized by sink_attn_workspace_bytes(params, 1)), and
+ * leaves q, k and the workspace unchanged in between; the workspace must not
+ * be in use by an earlier backward that is still running. Arguments and error
+ * behaviour as sink_attn_bwd_main. */
+SINK_API sink_status_t sink_attn_bwd_prepare(const sink_attn_params_t* params,
+                                    const void* q, const void* k,
+                                    void* workspace, size_t workspace_bytes, sink_stream_t stream);
+
+/* options bits of sink_attn_bwd_main_ex */
+#define SINK_BWD_PREPARED 1u /* sink_attn_bwd_prepare already ran on this workspace */
+
+/* sink_attn_bwd_main with options: options = 0 is exactly sink_attn_bwd_main;
+ * SINK_BWD_PREPARED skips the preparation pass (see sink_attn_bwd_prepare).
+ * Unknown option bits return SINK_ERR_INVALID_ARG. */
+SINK_API sink_status_t sink_attn_bwd_main_ex(const sink_attn_params_t* params,
+                                    const void* q, const void* k, const void* v,
+                                    const int32_t* cu_seqlens, const float* lse,
+                                    const float* delta, const void* dout,
+                                    void* dq, void* dk, void* dv,
+                                    void* workspace, size_t workspace_bytes,
+                                    unsigned options, sink_stream_t stream);
+
 /* Reads and clears the device flag word at the start of a workspace that was
  * passed to the calls above. SYNCHRONISES the stream (it copies 4 bytes back).
  * Returns SINK_OK, SINK_ERR_TIMEOUT (SINK_FLAG_TIMEOUT is set: outputs of that

@@ -97,6 +97,21 @@ def test_missing_workspace_rejected(L):
     assert L.sink_attn_fetch_device_error(nul, 0, nul, None) == _abi.SINK_ERR_WORKSPACE
 
 
+def test_split_preparation_entry_points_validate(L):
+    """sink_attn_bwd_prepare / sink_attn_bwd_main_ex: unknown option bits and
+    a missing workspace are rejected before anything touches the device."""
+    p = _params()
+    nul = ctypes.c_void_p(0)
+    assert L.sink_attn_bwd_main_ex(ctypes.byref(p), *([nul] * 10), nul, 0, 2, nul) == \
+        _abi.SINK_ERR_INVALID_ARG
+    assert L.sink_attn_bwd_main_ex(ctypes.byref(p), *([nul] * 10), nul, 0,
+                                   _abi.SINK_BWD_PREPARED, nul) == _abi.SINK_ERR_WORKSPACE
+    assert L.sink_attn_bwd_prepare(ctypes.byref(p), nul, nul, nul, 0, nul) == _abi.SINK_ERR_WORKSPACE
+    bad = _params(h_kv=3)  # 64 query heads do not group over 3
+    assert L.sink_attn_bwd_prepare(ctypes.byref(bad), nul, nul, nul, 0, nul) == \
+        _abi.SINK_ERR_INVALID_ARG
+
+
 def test_host_memory_workspace_rejected(L):
     """A host buffer is never handed to a kernel: the call fails up front."""
     p = _params()
@@ -141,6 +156,7 @@ def test_wait_limit_setter_round_trip(L):
 
 def test_flag_bits_match_the_header(L):
     text = open(os.path.join(ROOT, "include", "sink_attn.h"), encoding="utf-8").read()
-    for name in ("SINK_FLAG_TIMEOUT", "SINK_FLAG_SEQ_TOO_LONG", "SINK_FLAG_BAD_SEQLENS"):
+    for name in ("SINK_FLAG_TIMEOUT", "SINK_FLAG_SEQ_TOO_LONG", "SINK_FLAG_BAD_SEQLENS",
+                 "SINK_BWD_PREPARED"):
         m = re.search(rf"#define {name} (\d+)u", text)
         assert m and int(m.group(1)) == getattr(_abi, name)
