@@ -76,23 +76,28 @@ __device__ __forceinline__ bool seq_bounds_checked(const Problem& P, int s, int&
 }
 
 // This block's (x, y, z) for a grid of (row or key blocks, heads, sequences),
-// read from the linear launch index with z (the sequence) slowest, then x,
-// then y (the head) fastest. Blocks are dispatched roughly in linear-index
+// read from the linear launch index with z (the sequence) slowest, then
+// groups of G heads (G = 4 when the head count allows), then x, then the head
+// within its group fastest. Blocks are dispatched roughly in linear-index
 // order with x fastest; under a causal mask a block's work depends on its x,
 // and with x fastest every (head, sequence) slice ran long-to-short in turn,
 // so the last slice's longest blocks started late and most SMs idled while
-// they finished. With the heads innermost, the blocks of one sequence run
-// longest-first across all heads, and one sequence's Q / dO stay the working
-// set in L2 (an order with x slowest over all sequences spread the working set
-// over every packed sequence at once).
+// they finished. With a few heads innermost, the blocks of one sequence run
+// longest-first and the last blocks to start are short; grouping the heads
+// keeps the Q / dO rows and dQ accumulator lines that run at the same time to
+// a part of the sequence's heads, so more of them stay in L2 (an order with x
+// slowest over every sequence and head spread that set over all of them).
 struct BlockCoord {
     int x, y, z;
 };
 __device__ __forceinline__ BlockCoord block_seq_x_head() {
     const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-    const unsigned xy = gridDim.x * gridDim.y;
+    const unsigned X = gridDim.x, Y = gridDim.y;
+    const unsigned G = Y <= 4 ? Y : (Y % 4 == 0 ? 4 : (Y % 2 == 0 ? 2 : 1));
+    const unsigned xy = X * Y;
     const unsigned r = lin % xy;
-    return BlockCoord{(int)(r / gridDim.y), (int)(r % gridDim.y), (int)(lin / xy)};
+    const unsigned g = r / (G * X), r2 = r % (G * X);
+    return BlockCoord{(int)(r2 / G), (int)(g * G + r2 % G), (int)(lin / xy)};
 }
 
 // First allowed key of row i.
