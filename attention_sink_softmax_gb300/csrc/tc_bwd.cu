@@ -186,7 +186,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int nq = qb_hi - qb_lo + 1;
     const int nsteps = nq * P.group;
 
-    if (threadIdx.x == 0) {
+    // The elementwise threads fetch their key's K row (warpgroup 0, from the
+    // f16 copy) or V row (warpgroup 1) now, and the producer thread
+    // initialises the barriers and starts the K tile's load, so both are in
+    // flight while warp 0 allocates tensor memory.
+    uint32_t kv_row[32];
+    if (warp < 8) {
+        const int kp = k0 + (warp % 4) * 32 + lane;
+        const __nv_bfloat16* src = (warp < 4 ? kg : vg) + ((size_t)(start + kp) * P.h_kv + hk) * kD;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 x = kp < L ? __ldg(reinterpret_cast<const uint4*>(src) + j) : make_uint4(0, 0, 0, 0);
+            kv_row[4 * j] = x.x;
+            kv_row[4 * j + 1] = x.y;
+            kv_row[4 * j + 2] = x.z;
+            kv_row[4 * j + 3] = x.w;
+        }
+    }
+    if (threadIdx.x == 8 * 32) {
         mbar_init(&sm.k_full, 1);
         mbar_init(&sm.kv_tmem, 256);
         for (int i = 0; i < kQStages; ++i) {
@@ -208,6 +225,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(&sm.drained[1], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmDO);
+        mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
+        tma_load_3d(sm.k, &tmK, &sm.k_full, 0, hk, start + k0);
     }
     if (warp == 0) tmem_alloc<512>(&sm.tmem_slot);
     tc_fence_before();
@@ -226,19 +248,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const float sc = P.scale_log2;
         {
-            // A operands of S^T and dP^T: warpgroup 0 places this key's K row (f16,
-            // from the f16 copy), warpgroup 1 its V row (bf16); zeros past the sequence
-            uint32_t row[32];
-            const __nv_bfloat16* src = (w == 0 ? kg : vg) + ((size_t)(start + kp) * P.h_kv + hk) * kD;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 x = kp < L ? __ldg(reinterpret_cast<const uint4*>(src) + j) : make_uint4(0, 0, 0, 0);
-                row[4 * j] = x.x;
-                row[4 * j + 1] = x.y;
-                row[4 * j + 2] = x.z;
-                row[4 * j + 3] = x.w;
-            }
-            tmem_st32(tmem + lane_off + (w == 0 ? kColK : kColV), row);
+            // A operands of S^T and dP^T: warpgroup 0 places this key's K row (f16),
+            // warpgroup 1 its V row (bf16), loaded above; zeros past the sequence
+            tmem_st32(tmem + lane_off + (w == 0 ? kColK : kColV), kv_row);
             if (w == 0) {
                 // A of the extra K step: 1 in k = 0, 1, 2 of this key's row
                 uint8_t* ones = sm.aug_ones + aug_off(kr);
@@ -429,13 +441,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         regs_decrease<kCtlRegs>();
         if (warp == 8) {
             // -------------------------------------------------------- producer
-            if (lane == 0) {
-                tma_prefetch_desc(&tmQ);
-                tma_prefetch_desc(&tmK);
-                tma_prefetch_desc(&tmDO);
-                mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
-                tma_load_3d(sm.k, &tmK, &sm.k_full, 0, hk, start + k0);
-            }
+            // (the K tile's load went out before the CTA barrier)
             // B tiles of the extra K step: only k = 0..3 of each row are rewritten per step
             for (int i = lane; i < (int)(kQStages * kAugTile / 16); i += 32) {
                 reinterpret_cast<uint4*>(sm.aug_lse)[i] = make_uint4(0u, 0u, 0u, 0u);
