@@ -538,7 +538,7 @@ def run_reference(args, w, window):
 
 # ----------------------------------------------------------------------------- GPU arm
 def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo, lse, dq,
-            dk, dv, dsinks, delta, work, flops_step):
+            dk, dv, dsinks, delta, work_f, work, flops_step):
     """Same step through the public API with pinned host buffers: every step's
     inputs are copied in and every output copied back inside the timed region,
     as a training loop runs it: the next step's inputs are copied in on one
@@ -577,7 +577,7 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
             stream.wait_event(out_done[b])  # step i-2's outputs have been copied out
         if "o_lo" in dout_:
             sa.sink_attn_fwd_ex(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
-                                o_lo=dout_["o_lo"], lse=dout_["lse"], workspace=work, params=p,
+                                o_lo=dout_["o_lo"], lse=dout_["lse"], workspace=work_f, params=p,
                                 stream=stream)
             if args.serial_prepare:
                 sa.sink_attn_bwd_ex(din["q"], din["k"], din["v"], din["sinks"], dout_["o"],
@@ -603,7 +603,7 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
                 bwd_done.record(stream)
         else:
             sa.sink_attn_fwd(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
-                             lse=dout_["lse"], workspace=work, params=p, stream=stream)
+                             lse=dout_["lse"], workspace=work_f, params=p, stream=stream)
             sa.sink_attn_bwd(din["q"], din["k"], din["v"], din["sinks"], dout_["o"], dout_["lse"],
                              din["dout"], cu, dq=dout_["dq"], dk=dout_["dk"], dv=dout_["dv"],
                              dsinks=dout_["dsinks"], workspace=work, params=p, stream=stream)
@@ -637,6 +637,32 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
 
 
 
+def check_step_outputs(sa, p, q, k, v, sinks, dout, cu, o, lse, dq, dk, dv, dsinks, stream):
+    """The last timed step's outputs against one step run on the one stream
+    with fresh buffers: O, LSE, dK, dV and dS_h bit for bit, dQ (fp32 reduce-adds
+    in a varying order) within 2e-2 plus two ulps of its dtype. Guards the
+    timed step's concurrency (the preparation beside the forward)."""
+    with torch.cuda.stream(stream):
+        if q.dtype == torch.bfloat16:
+            o2, o_lo2, lse2 = sa.sink_attn_fwd_ex(q, k, v, sinks, cu, params=p)
+            dq2, dk2, dv2, ds2 = sa.sink_attn_bwd_ex(q, k, v, sinks, o2, o_lo2, lse2, dout, cu,
+                                                     params=p)
+        else:
+            o2, lse2 = sa.sink_attn_fwd(q, k, v, sinks, cu, params=p)
+            dq2, dk2, dv2, ds2 = sa.sink_attn_bwd(q, k, v, sinks, o2, lse2, dout, cu, params=p)
+    torch.cuda.synchronize()
+    for name, a, b in (("o", o, o2), ("lse", lse, lse2), ("dk", dk, dk2), ("dv", dv, dv2),
+                       ("dsinks", dsinks, ds2)):
+        if not torch.equal(a, b):
+            raise RuntimeError(f"timed step's {name} differs from a one-stream step")
+    # two runs of the fused backward differ by the order of their fp32 dQ
+    # reduce-adds, which can move a bf16 result by an ulp or two
+    a, b = dq.float(), dq2.float()
+    ulp = torch.ldexp(torch.ones_like(b), torch.frexp(b)[1] - (8 if dq.dtype == torch.bfloat16 else 24))
+    if ((a - b).abs() - (2e-2 + 2 * ulp)).max().item() > 0:
+        raise RuntimeError("timed step's dq differs from a one-stream step")
+
+
 def run_gpu(args, w, window):
     import attention_sink_softmax_gb300 as sa
 
@@ -660,8 +686,10 @@ def run_gpu(args, w, window):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dsinks = torch.empty_like(sinks)
     delta = torch.empty(p.h_q, p.total_tokens, dtype=torch.float32, device=dev)
-    wsz = max(sa.sink_attn_workspace_bytes(p, False), sa.sink_attn_workspace_bytes(p, True))
-    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    # the forward's and the backward's workspaces are separate buffers: the
+    # backward's preparation writes its workspace while the forward runs
+    work_f = torch.empty(sa.sink_attn_workspace_bytes(p, False), dtype=torch.uint8, device=dev)
+    work = torch.empty(sa.sink_attn_workspace_bytes(p, True), dtype=torch.uint8, device=dev)
 
     bwd_done = torch.cuda.Event()
     bwd_done.record(stream)
@@ -671,10 +699,10 @@ def run_gpu(args, w, window):
         if ev is not None:
             ev[0].record(stream)
         if o_lo is not None:
-            sa.sink_attn_fwd_ex(q, k, v, sinks, cu, out=o, o_lo=o_lo, lse=lse, workspace=work,
+            sa.sink_attn_fwd_ex(q, k, v, sinks, cu, out=o, o_lo=o_lo, lse=lse, workspace=work_f,
                                 params=p, stream=stream)
         else:
-            sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work, params=p,
+            sa.sink_attn_fwd(q, k, v, sinks, cu, out=o, lse=lse, workspace=work_f, params=p,
                              stream=stream)
         if overlap:
             # q and k are the step's inputs; the workspace's last user is the
@@ -701,12 +729,16 @@ def run_gpu(args, w, window):
             ev[3].record(stream)
         bwd_done.record(stream)
 
+    def check_flags(when):
+        for buf in (work_f, work):
+            st, flags = sa.sink_attn_fetch_device_error(buf)
+            if st != 0:
+                raise RuntimeError(f"device flagged an error {when}: status {st}, flags {flags}")
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    st, flags = sa.sink_attn_fetch_device_error(work)
-    if st != 0:
-        raise RuntimeError(f"device flagged an error during warm-up: status {st}, flags {flags}")
+    check_flags("during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -727,9 +759,8 @@ def run_gpu(args, w, window):
     ms_local = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms_local, ws, dev)
     stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j in range(3)]
-    st, flags = sa.sink_attn_fetch_device_error(work)
-    if st != 0:
-        raise RuntimeError(f"device flagged an error: status {st}, flags {flags}")
+    check_flags("in the timed steps")
+    check_step_outputs(sa, p, q, k, v, sinks, dout, cu, o, lse, dq, dk, dv, dsinks, stream)
 
     f_fwd, f_bwd = flops_of(w, window)
     flops_step = f_fwd + f_bwd
@@ -739,7 +770,7 @@ def run_gpu(args, w, window):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p, o, o_lo,
-                      lse, dq, dk, dv, dsinks, delta, work, flops_step)
+                      lse, dq, dk, dv, dsinks, delta, work_f, work, flops_step)
 
     pk, pk_src = peaks()
     # per-stage rates: FLOP/s (backward also without the S recompute, 8 d per

@@ -221,8 +221,10 @@ SINK_API sink_status_t sink_attn_bwd_main(const sink_attn_params_t* params,
  * SINK_BWD_PREPARED, which skips the pass.
  * The caller orders the two calls (an event), passes both the same params,
  * q, k and workspace (sized by sink_attn_workspace_bytes(params, 1)), and
- * leaves q, k and the workspace unchanged in between; the workspace must not
- * be in use by an earlier backward that is still running. Arguments and error
+ * leaves q, k and the workspace unchanged in between. No call that can run at
+ * the same time as the preparation may use that workspace: the forward it
+ * overlaps needs a workspace of its own (a different buffer), and an earlier
+ * backward on the same workspace must have finished. Arguments and error
  * behaviour as sink_attn_bwd_main. */
 SINK_API sink_status_t sink_attn_bwd_prepare(const sink_attn_params_t* params,
                                     const void* q, const void* k,
