@@ -100,6 +100,18 @@ __device__ __forceinline__ BlockCoord block_seq_x_head() {
     return BlockCoord{(int)(r2 / G), (int)(g * G + r2 % G), (int)(lin / xy)};
 }
 
+// Programmatic dependent launch. A kernel launched by launch_after() may begin
+// while the kernel before it in the stream is finishing (its CTAs take the SMs
+// that kernel's last wave leaves, and do their set-up); it calls pdl_wait()
+// before it reads anything that kernel wrote, which returns once that kernel
+// has completed and its writes are visible (at once in a normal launch). A
+// kernel calls pdl_trigger() when the next kernel may be scheduled: every
+// kernel that calls it does so as soon as its CTAs start. Only kernels
+// launched back to back inside one library call are launched this way, so
+// the kernel before one is always this library's.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // First allowed key of row i.
 __device__ __forceinline__ int key_lo(const Problem& P, int i) {
     if (!P.causal) return 0;

@@ -28,6 +28,7 @@ constexpr int kConvItems = 256 * kConvPerThread;
 
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ src,
                                                           uint4* __restrict__ dst, size_t n16) {
+    pdl_trigger();  // the forward that reads dst may take the SMs this grid frees
     const size_t base = (size_t)blockIdx.x * kConvItems + threadIdx.x;
 #pragma unroll
     for (int j = 0; j < kConvPerThread; ++j) {

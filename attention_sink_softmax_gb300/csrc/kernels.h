@@ -11,6 +11,25 @@ namespace sinkattn {
 // Counts every kernel launch the library enqueues (sink_attn_kernel_launches).
 void count_launches(unsigned n);
 
+// Launch `kernel` so that it may start while the previous kernel in `st` (one
+// this library launched in the same call) is finishing; the kernel calls
+// pdl_wait() before it reads that kernel's outputs (common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // f16 copy of `elems` bf16 values (a multiple of 8; 16-byte aligned buffers),
 // exact within f16's range (convert.cu).
 cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st);

@@ -75,6 +75,7 @@ preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restri
     constexpr int kIters = kPreTokens / kRowsPerIter;
     constexpr int kBatch = 4;  // rows of a thread in flight at once (3 blocks per SM for bf16)
     static_assert(kIters % kBatch == 0, "row batches");
+    pdl_trigger();  // the fixed-order dS_h sum may be scheduled
     __shared__ float warp_sum[kPreThreads / 32];
     const int h = blockIdx.x;
     const int nchunks = (total + kPreTokens - 1) / kPreTokens;
@@ -133,6 +134,7 @@ preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restri
 // dsinks[h] = -sum over chunks (in chunk order) of the partials.
 __global__ void dsink_reduce_kernel(int h_q, int nchunks, const float* __restrict__ partial,
                                     float* __restrict__ dsinks) {
+    pdl_wait();  // the partials of preprocess_kernel
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= h_q) return;
     float acc = 0.f;
@@ -174,9 +176,16 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    dsink_reduce_kernel<<<(P.h_q + 127) / 128, 128, 0, st>>>(P.h_q, nchunks, partial, dsinks);
+    // right after preprocess_kernel of this call: it may start while that kernel finishes
+    const dim3 grid((P.h_q + 127) / 128), block(128);
+    cudaError_t e = cudaSuccess;
+    if (nchunks > 0)
+        e = launch_after(dsink_reduce_kernel, grid, block, 0, st, P.h_q, nchunks,
+                         (const float*)partial, dsinks);
+    else
+        dsink_reduce_kernel<<<grid, block, 0, st>>>(P.h_q, nchunks, partial, dsinks);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 

@@ -185,6 +185,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // launched right after this call's conversion of V: its f16 copy is read below
+    pdl_wait();
     const uint32_t tmem = sm.tmem_slot;
     volatile int* abort_word = &sm.abort_flag;
 
@@ -536,6 +538,8 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // launched right after this call's conversion of V: its f16 copy is read below
+    pdl_wait();
     const uint32_t tmem = sm.tmem_slot;
     volatile int* abort_word = &sm.abort_flag;
 
@@ -917,10 +921,11 @@ static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUt
         fwd_tc_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid((P.max_seqlen + kBM - 1) / kBM, P.h_q / NT, P.nseq);
-    fwd_tc_kernel<NT, D><<<grid, fwd_threads<NT>(), smem, st>>>(
-        mq, mk, mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
+    // right after the conversion of V (tc_fwd): may start while it finishes
+    cudaError_t le = launch_after(fwd_tc_kernel<NT, D>, grid, dim3(fwd_threads<NT>()), smem, st, mq, mk, mv,
+                                  P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
     count_launches(1);
-    return cudaGetLastError();
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 template <int NT>
@@ -940,10 +945,10 @@ static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, con
     if (attr_err != cudaSuccess) return attr_err;
     const int nrb = (P.max_seqlen + kBM - 1) / kBM;
     dim3 grid((nrb + kWindowTiles - 1) / kWindowTiles, P.h_q / NT, P.nseq);
-    fwd_tc_tiles_kernel<NT><<<grid, fwd_threads<NT>(), smem, st>>>(
-        mq, mk, mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
+    cudaError_t le = launch_after(fwd_tc_tiles_kernel<NT>, grid, dim3(fwd_threads<NT>()), smem, st, mq, mk,
+                                  mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
     count_launches(1);
-    return cudaGetLastError();
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v,
