@@ -202,11 +202,11 @@ sink_status_t sink_attn_bwd_preprocess_ex(const sink_attn_params_t* params, cons
                  (params->total_tokens > 0 && !all_aligned({o_lo}))))
         return SINK_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return SINK_ERR_CUDA;
     const Problem P = make_problem(params, nullptr);
-    e = bwd_preprocess(P, params->dtype == SINK_BF16, sinks, o, o_lo, lse, dout, delta, dsinks,
-                       (float*)((char*)workspace + L.partial), s);
+    // the workspace's flag word is cleared by the call's last kernel
+    cudaError_t e = bwd_preprocess(P, params->dtype == SINK_BF16, sinks, o, o_lo, lse, dout, delta,
+                                   dsinks, (float*)((char*)workspace + L.partial),
+                                   (uint32_t*)workspace, s);
     return cuda_status(e);
 }
 

@@ -52,9 +52,11 @@ cudaError_t simt_bwd_main(const Problem& P, bool bf16, const void* q, const void
 int preprocess_chunks(int total);
 // o_lo (nullable, bf16 only): the low-order part of O written by the forward;
 // when given, delta = dout . (o + o_lo).
+// clear_flags (nullable): a device flag word zeroed before the call returns
+// control to the stream's next kernel (the backward's own flags).
 cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, const void* o,
                            const void* o_lo, const float* lse, const void* dout, float* delta,
-                           float* dsinks, float* partial, cudaStream_t st);
+                           float* dsinks, float* partial, uint32_t* clear_flags, cudaStream_t st);
 
 // Decode (decode.cu): split kernel (+ merge kernel on the CUDA-core path).
 // `part` holds decode_partial_floats(batch, h_q) floats; `counters` holds

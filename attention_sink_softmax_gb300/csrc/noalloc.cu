@@ -98,7 +98,7 @@ sink_status_t sink_attn_bwd_preprocess_noalloc(const sink_attn_params_t* p, cons
     P.head_dim = p->head_dim;
     P.wait_ns = kDefaultWaitNs;
     cudaError_t e = bwd_preprocess(P, p->dtype == SINK_BF16, sinks, o, nullptr, lse, dout, delta,
-                                   dsinks, scratch, (cudaStream_t)stream);
+                                   dsinks, scratch, nullptr, (cudaStream_t)stream);
     return e == cudaSuccess ? SINK_OK : SINK_ERR_CUDA;
 }
 

@@ -131,15 +131,23 @@ preprocess_kernel(int total, int h_q, const T* __restrict__ o, const T* __restri
     }
 }
 
-// dsinks[h] = -sum over chunks (in chunk order) of the partials.
+// dsinks[h] = -(sum of the per-chunk partials of head h): one warp per head,
+// lane l adds chunks l, l + 32, l + 64, ... in order, then the 32 lane sums
+// are combined by a fixed butterfly, so the result is the same on every run.
+// clear_flags (nullable): the workspace's device flag word, zeroed here so
+// that the backward kernels after this one report their own conditions.
 __global__ void dsink_reduce_kernel(int h_q, int nchunks, const float* __restrict__ partial,
-                                    float* __restrict__ dsinks) {
+                                    float* __restrict__ dsinks, uint32_t* clear_flags) {
     pdl_wait();  // the partials of preprocess_kernel
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (clear_flags && blockIdx.x == 0 && threadIdx.x == 0) *clear_flags = 0u;
+    const int h = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
     if (h >= h_q) return;
     float acc = 0.f;
-    for (int c = 0; c < nchunks; ++c) acc += partial[(size_t)h * nchunks + c];
-    dsinks[h] = -acc;
+    for (int c = lane; c < nchunks; c += 32) acc += partial[(size_t)h * nchunks + c];
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (lane == 0) dsinks[h] = -acc;
 }
 
 
@@ -159,7 +167,7 @@ static void launch_preprocess(dim3 grid, cudaStream_t st, const Problem& P, cons
 
 cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, const void* o,
                            const void* o_lo, const float* lse, const void* dout, float* delta,
-                           float* dsinks, float* partial, cudaStream_t st) {
+                           float* dsinks, float* partial, uint32_t* clear_flags, cudaStream_t st) {
     const int nchunks = preprocess_chunks(P.total);
     if (nchunks > 0) {
         dim3 grid(P.h_q, nchunks < 65535 ? nchunks : 65535);
@@ -177,13 +185,13 @@ cudaError_t bwd_preprocess(const Problem& P, bool bf16, const float* sinks, cons
         if (e != cudaSuccess) return e;
     }
     // right after preprocess_kernel of this call: it may start while that kernel finishes
-    const dim3 grid((P.h_q + 127) / 128), block(128);
+    const dim3 grid((P.h_q + 3) / 4), block(128);  // one warp per head
     cudaError_t e = cudaSuccess;
     if (nchunks > 0)
         e = launch_after(dsink_reduce_kernel, grid, block, 0, st, P.h_q, nchunks,
-                         (const float*)partial, dsinks);
+                         (const float*)partial, dsinks, clear_flags);
     else
-        dsink_reduce_kernel<<<grid, block, 0, st>>>(P.h_q, nchunks, partial, dsinks);
+        dsink_reduce_kernel<<<grid, block, 0, st>>>(P.h_q, nchunks, partial, dsinks, clear_flags);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
