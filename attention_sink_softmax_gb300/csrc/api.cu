@@ -167,15 +167,15 @@ sink_status_t sink_attn_fwd_ex(const sink_attn_params_t* params, const void* q, 
     if ((st = check_o_lo(params, o_lo)) != SINK_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t* flags = (uint32_t*)workspace;
-    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess || empty(params)) return cuda_status(e);
     const Problem P = make_problem(params, cu_seqlens);
     const bool bf16 = params->dtype == SINK_BF16;
-    if (tc_fwd_supported(P, bf16))
-        e = tc_fwd(P, q, k, v, sinks, o, o_lo, lse, flags, (char*)workspace + kHeaderBytes, s);
-    else
-        e = simt_fwd(P, bf16, q, k, v, sinks, o, o_lo, lse, flags, s);
-    return cuda_status(e);
+    // the tensor-core path's first kernel (V's f16 copy) zeroes the flag word
+    if (!empty(params) && tc_fwd_supported(P, bf16))
+        return cuda_status(tc_fwd(P, q, k, v, sinks, o, o_lo, lse, flags,
+                                  (char*)workspace + kHeaderBytes, s));
+    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess || empty(params)) return cuda_status(e);
+    return cuda_status(simt_fwd(P, bf16, q, k, v, sinks, o, o_lo, lse, flags, s));
 }
 
 sink_status_t sink_attn_fwd(const sink_attn_params_t* params, const void* q, const void* k,

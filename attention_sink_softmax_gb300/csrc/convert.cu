@@ -27,7 +27,15 @@ constexpr int kConvPerThread = 8;
 constexpr int kConvItems = 256 * kConvPerThread;
 
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ src,
-                                                          uint4* __restrict__ dst, size_t n16) {
+                                                          uint4* __restrict__ dst, size_t n16,
+                                                          uint32_t* clear_flags) {
+    if (clear_flags && blockIdx.x == 0 && threadIdx.x == 0) {
+        // the forward's device flag word: zeroed and made visible before the
+        // forward (launched after this grid) may start and set a flag
+        *clear_flags = 0u;
+        __threadfence();
+    }
+    __syncthreads();
     pdl_trigger();  // the forward that reads dst may take the SMs this grid frees
     const size_t base = (size_t)blockIdx.x * kConvItems + threadIdx.x;
 #pragma unroll
@@ -90,13 +98,14 @@ cudaError_t bwd_prepare(const void* q, void* q16, size_t q_elems, const void* k,
     return cudaGetLastError();
 }
 
-cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st) {
+cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st,
+                                uint32_t* clear_flags) {
     const size_t n16 = elems / 8;  // callers pass whole rows of 64 or 128 elements
     if (n16 == 0) return cudaSuccess;
     const size_t blocks = (n16 + kConvItems - 1) / kConvItems;
     if (blocks > 0x7fffffffu) return cudaErrorInvalidValue;
     bf16_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(src),
-                                                static_cast<uint4*>(dst), n16);
+                                                          static_cast<uint4*>(dst), n16, clear_flags);
     count_launches(1);
     return cudaGetLastError();
 }

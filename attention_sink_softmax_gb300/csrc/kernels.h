@@ -32,7 +32,10 @@ cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t
 
 // f16 copy of `elems` bf16 values (a multiple of 8; 16-byte aligned buffers),
 // exact within f16's range (convert.cu).
-cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st);
+// clear_flags (nullable): a device flag word zeroed by the kernel before the
+// next kernel (launched with launch_after) may start.
+cudaError_t convert_bf16_to_f16(const void* src, void* dst, size_t elems, cudaStream_t st,
+                                uint32_t* clear_flags = nullptr);
 // f16 copies of q (q_elems) and k (k_elems) and acc_floats zeros, in one pass
 // (the 64-wide tensor-core backward's preparation; convert.cu).
 cudaError_t bwd_prepare(const void* q, void* q16, size_t q_elems, const void* k, void* k16,

@@ -957,7 +957,8 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
     if (P.nseq == 0 || P.max_seqlen == 0) return cudaSuccess;
     // V in f16 for the P V product (the same 2-byte layout; TMA copies bytes)
     void* v16 = workspace;
-    cudaError_t e = convert_bf16_to_f16(v, v16, (size_t)P.total * P.h_kv * P.head_dim, st);
+    // (the conversion also zeroes the workspace's flag word for the forward)
+    cudaError_t e = convert_bf16_to_f16(v, v16, (size_t)P.total * P.h_kv * P.head_dim, st, flags);
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv;
     if (!make_head_tile_map(&mq, q, P.total, P.h_q, kBM, P.head_dim) ||
