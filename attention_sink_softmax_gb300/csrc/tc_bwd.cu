@@ -297,14 +297,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (q0 + kBM > L ||
                 (P.causal ? (k0 + kBN - 1 > q0 || (P.window > 0 && k0 < q0 + kBM - P.window))
                           : (k0 + kBN > L))) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const int ip = q0 + 64 * w + j;
-                    const bool allowed =
-                        ip < L && (P.causal ? (kp <= ip && (P.window <= 0 || kp > ip - P.window))
-                                            : kp < L);
-                    p[j] = allowed ? p[j] : 0.f;
+                // this key is seen by the query rows ip with ip >= kp (causal),
+                // ip < kp + window and ip < L: as offsets j = ip - base from this
+                // thread's first row, the interval [lo, hi), two compares per element
+                const int base = q0 + 64 * w;
+                int lo = 0, hi = L - base;
+                if (P.causal) {
+                    lo = kp - base;
+                    if (P.window > 0) hi = min(hi, kp + P.window - base);
+                } else if (kp >= L) {
+                    hi = lo;
                 }
+#pragma unroll
+                for (int j = 0; j < 64; ++j) p[j] = (j >= lo && j < hi) ? p[j] : 0.f;
             }
             // packed pairs: P^T in bf16 (tensor memory, A of dV), dS^T in f16 (tensor
             // memory, A of dK, and shared memory, A of dQ; their B operands Q and K
