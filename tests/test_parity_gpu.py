@@ -59,6 +59,9 @@ CASES = [
     ([333, 190], 6, 2, True, True, 0),         # group of 3: the forward's odd-group CTAs
     ([700], 5, 1, True, True, 4096),           # group of 5, window longer than the sequence
     ([900, 260], 14, 2, True, True, 640),      # group of 7, window 640
+    ([700, 301], 6, 2, True, True, 256),       # window 256 (the multi-tile forward's limit), group of 3
+    ([513, 129], 8, 2, True, True, 256),       # window 256, pairs of query heads, ragged tails
+    ([600, 77], 8, 2, True, True, 257),        # just above it: the one-tile forward with a window
 ]
 
 
