@@ -128,18 +128,6 @@ __device__ __forceinline__ uint32_t sw128(int r, int b) {
     return (uint32_t)(r * 128 + (((b >> 4) ^ (r & 7)) << 4) + (b & 15));
 }
 
-// AND of `pred` over the 128 threads of named barrier `id` (all of them must call it)
-__device__ __forceinline__ bool vote_all_128(int id, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-        "barrier.cta.red.and.pred po, %2, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"((uint32_t)pred), "r"(id)
-        : "memory");
-    return out != 0;
-}
-
 __device__ __forceinline__ uint4 pack8(const uint32_t* a, float f) {
     return make_uint4(pack_bf16x2(__uint_as_float(a[0]) * f, __uint_as_float(a[1]) * f),
                       pack_bf16x2(__uint_as_float(a[2]) * f, __uint_as_float(a[3]) * f),

@@ -44,6 +44,7 @@
 // At D = 128 a CTA holds one tile (NT = 1): S 128 + O 128 + P 64 columns.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -76,25 +77,37 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 384 * kLaunchRegs, "r
 template <int NT>
 constexpr int fwd_threads() { return NT * 128 + 128; }
 
-// Eight consecutive O values of a row, scaled by 1 / l, stored as bf16 at dst;
-// when dst_lo is given, the bf16 of what that rounding dropped (O - bf16(O),
-// exact in fp32) goes to dst_lo, so that o + o_lo carries about 16 bits of O.
-__device__ __forceinline__ void store_o8(uint4* dst, uint4* dst_lo, const uint32_t* a, float inv) {
+// Eight consecutive O values of a row, scaled by 1 / l: their bf16 (hi) and
+// the bf16 of what that rounding dropped (lo = O - bf16(O), exact in fp32), so
+// that o + o_lo carries about 16 bits of O.
+__device__ __forceinline__ void pack_o8(const uint32_t* a, float inv, uint4& hi_out, uint4& lo_out) {
     float x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(a[j]) * inv;
-    uint32_t hi[4];
+    uint32_t hi[4], lo[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-    *dst = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    if (dst_lo) {
-        uint32_t lo[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            lo[j] = pack_bf16x2(x[2 * j] - __uint_as_float(hi[j] << 16),
-                                x[2 * j + 1] - __uint_as_float(hi[j] & 0xFFFF0000u));
-        *dst_lo = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
+    for (int j = 0; j < 4; ++j)
+        lo[j] = pack_bf16x2(x[2 * j] - __uint_as_float(hi[j] << 16),
+                            x[2 * j + 1] - __uint_as_float(hi[j] & 0xFFFF0000u));
+    hi_out = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    lo_out = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Eight consecutive O values of a row, scaled by 1 / l, stored as bf16 at dst;
+// when dst_lo is given, the bf16 of what that rounding dropped goes to dst_lo.
+__device__ __forceinline__ void store_o8(uint4* dst, uint4* dst_lo, const uint32_t* a, float inv) {
+    uint4 hi, lo;
+    pack_o8(a, inv, hi, lo);
+    *dst = hi;
+    if (dst_lo) *dst_lo = lo;
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-row tile of 128-byte rows
+// with the 128-byte swizzle (the layout of a TMA box of 64 bf16 x 128 rows).
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // The sink's term joins the row's denominator once every key has been seen:
@@ -462,6 +475,8 @@ struct FwdTilesSmem {
     alignas(1024) __nv_bfloat16 q[2][NT][kBM * 64];
     alignas(1024) __nv_bfloat16 k[kStages][kBN * 64];
     alignas(1024) __nv_bfloat16 v[kStages][kBN * 64];
+    // tile t's normalised O and o_lo, staged for one TMA store each
+    alignas(1024) __nv_bfloat16 o_stage[NT][2][kBM * 64];
     uint64_t q_full[2], q_empty[2];
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[NT], s_loaded[NT], p_full[NT], o_done[NT];
@@ -476,7 +491,8 @@ static_assert(sizeof(FwdTilesSmem<2>) + 1024 <= 232448, "shared memory of the mu
 template <int NT>
 __global__ void __launch_bounds__(fwd_threads<NT>(), 1)
 fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const Problem P,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const __grid_constant__ CUtensorMap tmOlo, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
               __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, uint32_t* flags) {
     constexpr int D = 64;
@@ -671,16 +687,16 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             l = l * corr + rs;
             m = m_new;
         }
-        if (!ok) break;
-        ok = __all_sync(0xffffffffu, wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word, P.wait_ns));
+        // One decision for the tile's four warps, each of which reaches this
+        // point even when it gave up inside the block loop: they meet at the
+        // named barrier 1 + t below.
+        ok = vote_all_128(1 + t, ok && wait_phase(&sm.o_done[t], (g - 1) & 1, flags, abort_word,
+                                                  P.wait_ns));
         if (!ok) break;
         {
             tc_fence_after();
             float row_lse;
             const float inv = fold_sink(m, l, sink2, &row_lse);
-            const size_t ooff = ((size_t)(start + row) * P.h_q + h) * D;
-            uint4* dst = reinterpret_cast<uint4*>(out + ooff);
-            uint4* dst_lo = out_lo ? reinterpret_cast<uint4*>(out_lo + ooff) : nullptr;
             static_assert(D == 64, "the multi-tile forward is 64 wide");
             // both loads complete before any register they write is read
             uint32_t oa[32], ob[32];
@@ -690,7 +706,33 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // O_t is in registers: the next tile's first P V may overwrite it
             tc_fence_before();
             mbar_arrive(&sm.o_free[t]);
-            if (valid) {
+            if (r0 + kBM <= L) {
+                // a whole tile of the sequence: O and o_lo through shared memory
+                // and one TMA store each (rows leave as whole 128-byte lines
+                // instead of a 16-byte piece per thread per row)
+                uint8_t* so = reinterpret_cast<uint8_t*>(sm.o_stage[t][0]);
+                uint8_t* sl = reinterpret_cast<uint8_t*>(sm.o_stage[t][1]);
+                if (r == 0) bulk_wait_read<0>();  // the previous tile's stores have read them
+                named_barrier_sync(1 + t, 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 hi, lo;
+                    pack_o8(j < 4 ? oa + 8 * j : ob + 8 * (j - 4), inv, hi, lo);
+                    *reinterpret_cast<uint4*>(so + sw128_chunk(r, j)) = hi;
+                    *reinterpret_cast<uint4*>(sl + sw128_chunk(r, j)) = lo;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                named_barrier_sync(1 + t, 128);
+                if (r == 0) {
+                    tma_store_3d(&tmO, so, 0, h, start + r0);
+                    if (out_lo) tma_store_3d(&tmOlo, sl, 0, h, start + r0);
+                    bulk_commit();
+                }
+                lse[(size_t)h * P.total + start + row] = row_lse;
+            } else if (valid) {
+                const size_t ooff = ((size_t)(start + row) * P.h_q + h) * D;
+                uint4* dst = reinterpret_cast<uint4*>(out + ooff);
+                uint4* dst_lo = out_lo ? reinterpret_cast<uint4*>(out_lo + ooff) : nullptr;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     store_o8(dst + j, dst_lo ? dst_lo + j : nullptr, oa + 8 * j, inv);
@@ -700,6 +742,8 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         }
         }  // tiles
+        // the staged tiles' stores complete before the CTA's shared memory goes away
+        if (r == 0) bulk_wait_all<0>();
         } else {
         if (NT == 2) regs_decrease<kOtherRegs>();
         if (warp == 4 * NT) {
@@ -943,10 +987,17 @@ static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, con
     cudaError_t attr_err = cudaFuncSetAttribute(
         fwd_tc_tiles_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
+    // the epilogue's store maps: [T, H_q, 64] O and o_lo, 128-row boxes
+    CUtensorMap mo, mol;
+    memset(&mo, 0, sizeof(mo));
+    memset(&mol, 0, sizeof(mol));
+    if (!make_head_tile_map(&mo, o, P.total, P.h_q, kBM) ||
+        (o_lo && !make_head_tile_map(&mol, o_lo, P.total, P.h_q, kBM)))
+        return cudaErrorInvalidValue;
     const int nrb = (P.max_seqlen + kBM - 1) / kBM;
     dim3 grid((nrb + kWindowTiles - 1) / kWindowTiles, P.h_q / NT, P.nseq);
     cudaError_t le = launch_after(fwd_tc_tiles_kernel<NT>, grid, dim3(fwd_threads<NT>()), smem, st, mq, mk,
-                                  mv, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
+                                  mv, mo, mol, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
     count_launches(1);
     return le != cudaSuccess ? le : cudaGetLastError();
 }

@@ -93,6 +93,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
         "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// 3-D tiled store of a shared-memory box into global memory (bulk async group;
+// the innermost coordinate must be 16-byte aligned, none negative).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -108,6 +118,18 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// AND of `pred` over the 128 threads of named barrier `id` (all of them must call it)
+__device__ __forceinline__ bool vote_all_128(int id, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.cta.red.and.pred po, %2, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)pred), "r"(id)
+        : "memory");
+    return out != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05
