@@ -461,14 +461,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 // A short window (at most 256 keys) leaves each row tile one or two key
 // blocks, too little work to hide a CTA's start-up (tensor-memory allocation,
 // first loads, pipeline fill) and its epilogue. fwd_tc_tiles_kernel runs
-// kWindowTiles consecutive row tiles of the same query heads in one CTA: the
+// several consecutive row tiles of the same query heads in one CTA (a launch
+// parameter, fwd_tiles_per_cta below): the
 // next tile's Q is loaded into the second Q buffer while the current tile
 // computes, the K/V ring and the barrier phases run on across tiles (a block
 // counter g), and each tile's first P V waits until the softmax has read the
 // previous tile's O (o_free). It is the kernel above generalised to several
 // tiles; the one-tile kernel is kept separate because the generalised loops
 // cost it about 7 % on the causal layer. d = 64 only.
-constexpr int kWindowTiles = 4;
 
 template <int NT>
 struct FwdTilesSmem {
@@ -494,9 +494,9 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const __grid_constant__ CUtensorMap tmOlo, const Problem P,
               const float* __restrict__ sinks, __nv_bfloat16* __restrict__ out,
-              __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, uint32_t* flags) {
+              __nv_bfloat16* __restrict__ out_lo, float* __restrict__ lse, uint32_t* flags,
+              const int tiles_per_cta) {
     constexpr int D = 64;
-    constexpr int kTiles = kWindowTiles;
     constexpr int kQBufs = 2;
     constexpr int kAtoms = D / kAtomCols;
     constexpr uint32_t kTileBytes = tile_bytes<D>();
@@ -511,8 +511,8 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (!seq_bounds_checked(P, seq, start, L, flags)) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && L > P.max_seqlen) atomicOr(flags, kFlagSeqTooLong);
     // this CTA's row tiles: row blocks rb0 .. rb0 + ntile - 1 of the sequence
-    const int rb0 = cb * kTiles;
-    const int ntile = kTiles == 1 ? 1 : min(kTiles, (L + kBM - 1) / kBM - rb0);
+    const int rb0 = cb * tiles_per_cta;
+    const int ntile = min(tiles_per_cta, (L + kBM - 1) / kBM - rb0);
     if (rb0 * kBM >= L) return;  // uniform for the whole CTA, before any barrier or TMEM use
     // first row, first key block and number of key blocks of tile k
     auto tile_blocks = [&](int k, int& r0, int& kb_lo, int& nblk) {
@@ -972,6 +972,36 @@ static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUt
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
+// Row tiles per CTA of the multi-tile forward. More tiles spread a CTA's
+// start-up over more work; fewer leave more, shorter CTAs to fill the last
+// wave. The count minimises waves x (start-up + mean tiles per CTA) over
+// 4, 8, 12 and 16, the start-up counted as one tile's time and every sequence
+// taken at the mean length (cu_seqlens stays on the device); a tie goes to
+// the larger count. A list-scheduling model of the launch ranks the counts
+// the same way on the 4 x 8192 and the 48-sequence packed window layers,
+// where the measured best were 8 and 16.
+static int fwd_tiles_per_cta(const Problem& P, int nt) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    const long long mean_len = ((long long)P.total + P.nseq - 1) / P.nseq;
+    const long long nrb = mean_len > 0 ? (mean_len + kBM - 1) / kBM : 1;
+    const long long slices = (long long)(P.h_q / nt) * P.nseq;
+    int best = 4;
+    double best_est = 0.0;
+    for (int t = 4; t <= 16; t += 4) {
+        const long long per_seq = (nrb + t - 1) / t;
+        const long long waves = (per_seq * slices + sms - 1) / sms;
+        const double est = (double)waves * (1.0 + (double)nrb / (double)per_seq);
+        if (t == 4 || est <= best_est) {
+            best = t;
+            best_est = est;
+        }
+    }
+    return best;
+}
+
 template <int NT>
 static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, const CUtensorMap& mk,
                                     const CUtensorMap& mv, const float* sinks, void* o, void* o_lo,
@@ -995,9 +1025,11 @@ static cudaError_t launch_fwd_tiles(const Problem& P, const CUtensorMap& mq, con
         (o_lo && !make_head_tile_map(&mol, o_lo, P.total, P.h_q, kBM)))
         return cudaErrorInvalidValue;
     const int nrb = (P.max_seqlen + kBM - 1) / kBM;
-    dim3 grid((nrb + kWindowTiles - 1) / kWindowTiles, P.h_q / NT, P.nseq);
+    const int tiles = fwd_tiles_per_cta(P, NT);
+    dim3 grid((nrb + tiles - 1) / tiles, P.h_q / NT, P.nseq);
     cudaError_t le = launch_after(fwd_tc_tiles_kernel<NT>, grid, dim3(fwd_threads<NT>()), smem, st, mq, mk,
-                                  mv, mo, mol, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags);
+                                  mv, mo, mol, P, sinks, (__nv_bfloat16*)o, (__nv_bfloat16*)o_lo, lse, flags,
+                                  tiles);
     count_launches(1);
     return le != cudaSuccess ? le : cudaGetLastError();
 }
