@@ -296,8 +296,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 } else if (kp >= L) {
                     hi = lo;
                 }
+                // which bounds can cut into this half step's 64 rows for some key
+                // of the block (uniform over the warpgroup): on a window layer
+                // most half steps need only one of them
+                const bool need_lo = !P.causal || base < k0 + kBN - 1;
+                const bool need_hi = !P.causal || base + 63 >= L ||
+                                     (P.window > 0 && base + 63 >= k0 + P.window);
+                if (need_lo && need_hi) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) p[j] = (j >= lo && j < hi) ? p[j] : 0.f;
+                    for (int j = 0; j < 64; ++j) p[j] = (j >= lo && j < hi) ? p[j] : 0.f;
+                } else if (need_lo) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) p[j] = j >= lo ? p[j] : 0.f;
+                } else if (need_hi) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) p[j] = j < hi ? p[j] : 0.f;
+                }
             }
             // packed pairs: P^T in bf16 (tensor memory, A of dV), dS^T in f16 (tensor
             // memory, A of dK, and shared memory, A of dQ; their B operands Q and K

@@ -602,12 +602,28 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             (P.window > 0 && kp0 < r0 + kBM - P.window))
                          : (kp0 + kBN > L);
             if (need_mask) {
-                const int lo = P.causal && P.window > 0 ? row - P.window + 1 : INT_MIN;
-                const int hi = P.causal ? min(row, L - 1) : L - 1;
+                // (causal, with a window) a block needs the causal bound only if it
+                // reaches past the tile's first row, and the window bound only if
+                // it starts before the last row's window: on a window layer most
+                // blocks need one of the two, tested alone
+                const int lo = P.window > 0 ? row - P.window + 1 : INT_MIN;
+                const int hi = min(row, L - 1);
+                const bool need_hi = kp0 + kBN - 1 > r0;
+                const bool need_lo = P.window > 0 && kp0 < r0 + kBM - P.window;
+                if (need_hi && need_lo) {
 #pragma unroll
-                for (int j = 0; j < 128; ++j) {
-                    const int kp = kp0 + j;
-                    if (kp < lo || kp > hi) s[j] = -INFINITY;
+                    for (int j = 0; j < 128; ++j)
+                        if (kp0 + j < lo || kp0 + j > hi) s[j] = -INFINITY;
+                } else if (need_hi) {
+                    const int jh = hi - kp0;
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        if (j > jh) s[j] = -INFINITY;
+                } else {
+                    const int jl = lo - kp0;
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        if (j < jl) s[j] = -INFINITY;
                 }
             }
             // row max: three-input max, four independent chains
