@@ -20,7 +20,8 @@ GB/s, the backward also without the recompute), ``roofline`` for the dominant
 stage (the backward main loop; against HBM when its arithmetic intensity is
 below the ridge point, as in the window layers), ``e2e`` (the same step with
 inputs copied in from pinned host memory and every output copied back each
-step, the copies overlapping the neighbouring steps' compute), ``clocks``
+step, the copies overlapping the neighbouring steps' compute; the backward
+as one sink_attn_bwd_ex call, whose preparation runs inside it), ``clocks``
 sampled during the timed region and ``cpu_baseline`` (the oracle on the host
 cores, bounded sample).
 
@@ -544,7 +545,12 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
     as a training loop runs it: the next step's inputs are copied in on one
     stream and the previous step's outputs copied out on another while the
     current step computes (device buffers double-buffered, events order the
-    reuse). Timed from the first copy in to the last copy out."""
+    reuse). Timed from the first copy in to the last copy out.
+
+    The backward is the one-call sink_attn_bwd_ex unless --overlap-e2e asks
+    for the preparation on the side stream: with the host copies in flight
+    the overlapped form's time varied from run to run (from 4.2 to 5.5 ms a
+    step on one GB300, against 4.245 ms every time for the one call)."""
     import attention_sink_softmax_gb300 as sa
     host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
     outs0 = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dsinks": dsinks}
@@ -579,7 +585,7 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
             sa.sink_attn_fwd_ex(din["q"], din["k"], din["v"], din["sinks"], cu, out=dout_["o"],
                                 o_lo=dout_["o_lo"], lse=dout_["lse"], workspace=work_f, params=p,
                                 stream=stream)
-            if args.serial_prepare:
+            if args.serial_prepare or not args.overlap_e2e:
                 sa.sink_attn_bwd_ex(din["q"], din["k"], din["v"], din["sinks"], dout_["o"],
                                     dout_["o_lo"], dout_["lse"], din["dout"], cu, dq=dout_["dq"],
                                     dk=dout_["dk"], dv=dout_["dv"], dsinks=dout_["dsinks"],
@@ -633,7 +639,10 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
                                rtol=0, atol=0)
     return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-            "overlap": "copies in and out on their own streams, overlapping the neighbouring steps' compute"}
+            "overlap": "copies in and out on their own streams, overlapping the neighbouring steps' compute",
+            "bwd": ("sink_attn_bwd_prepare on the side stream, then sink_attn_bwd_main"
+                    if args.overlap_e2e and not args.serial_prepare and "o_lo" in dev_out[0]
+                    else "one sink_attn_bwd call")}
 
 
 
@@ -942,6 +951,9 @@ def main():
                          "case of the same layer, e.g. for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--overlap-e2e", action="store_true",
+                    help="end-to-end timing with the backward's preparation on the side stream "
+                         "(default: the one-call backward)")
     ap.add_argument("--serial-prepare", action="store_true",
                     help="run the backward preparation inside sink_attn_bwd_main on the step's "
                          "stream instead of beside the forward on a lower-priority one")
