@@ -467,8 +467,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 // computes, the K/V ring and the barrier phases run on across tiles (a block
 // counter g), and each tile's first P V waits until the softmax has read the
 // previous tile's O (o_free). It is the kernel above generalised to several
-// tiles; the one-tile kernel is kept separate because the generalised loops
-// cost it about 7 % on the causal layer. d = 64 only.
+// tiles, for causal layers (with or without a window) at d = 64; with two
+// tiles per CTA it is also faster than the one-tile kernel on a full causal
+// layer of moderate length (one CTA's start-up and epilogue per two tiles).
+// The one-tile kernel serves the other cases (no causal mask, an odd group,
+// rows longer than kTwoTileMaxRows).
 
 template <int NT>
 struct FwdTilesSmem {
@@ -602,10 +605,10 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             (P.window > 0 && kp0 < r0 + kBM - P.window))
                          : (kp0 + kBN > L);
             if (need_mask) {
-                // (causal, with a window) a block needs the causal bound only if it
-                // reaches past the tile's first row, and the window bound only if
-                // it starts before the last row's window: on a window layer most
-                // blocks need one of the two, tested alone
+                // (this kernel runs causal layers only) a block needs the causal
+                // bound only if it reaches past the tile's first row, and the
+                // window bound only if it starts before the last row's window: on
+                // a window layer most blocks need one of the two, tested alone
                 const int lo = P.window > 0 ? row - P.window + 1 : INT_MIN;
                 const int hi = min(row, L - 1);
                 const bool need_hi = kp0 + kBN - 1 > r0;
@@ -786,6 +789,12 @@ fwd_tc_tiles_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     q_issued = k + 1;
                     for (int i = 0; i < nblk; ++i, ++g) {
                         const int st = g % kStages;
+                        // test hook (off unless a test sets it): no load after the
+                        // CTA's first K/V stage, so the consumers' bounded waits run out
+                        if (P.withhold_load && g == 1) {
+                            ok = false;
+                            break;
+                        }
                         if (g >= kStages &&
                             !wait_phase(&sm.kv_empty[st], ((g / kStages) - 1) & 1, flags, abort_word, P.wait_ns)) {
                             ok = false;
@@ -988,15 +997,24 @@ static cudaError_t launch_fwd(const Problem& P, const CUtensorMap& mq, const CUt
     return le != cudaSuccess ? le : cudaGetLastError();
 }
 
-// Row tiles per CTA of the multi-tile forward. More tiles spread a CTA's
-// start-up over more work; fewer leave more, shorter CTAs to fill the last
-// wave. The count minimises waves x (start-up + mean tiles per CTA) over
-// 4, 8, 12 and 16, the start-up counted as one tile's time and every sequence
-// taken at the mean length (cu_seqlens stays on the device); a tie goes to
-// the larger count. A list-scheduling model of the launch ranks the counts
-// the same way on the 4 x 8192 and the 48-sequence packed window layers,
-// where the measured best were 8 and 16.
+// Row tiles per CTA of the multi-tile forward. Without a short window a tile
+// has up to max_seqlen / 128 key blocks and two tiles per CTA measured best
+// (four lengthened the causal 2 x 8192 forward by 5 %). With a window of at
+// most 256 keys, more tiles spread a CTA's start-up over more work and fewer
+// leave more, shorter CTAs to fill the last wave: the count minimises
+// waves x (start-up + mean tiles per CTA) over 4, 8, 12 and 16, the start-up
+// counted as one tile's time and every sequence taken at the mean length
+// (cu_seqlens stays on the device); a tie goes to the larger count. A
+// list-scheduling model of the launch ranks the counts the same way on the
+// 4 x 8192 and the 48-sequence packed window layers, where the measured best
+// were 8 and 16.
+// Rows up to which a causal layer without a short window runs two tiles per
+// CTA (measured: 2 x 8192 forward -1.1 %, 48 packed sequences of at most 8192
+// -7.8 %, 1 x 32768 +1.5 %; the limit lies between the last two).
+constexpr int kTwoTileMaxRows = 16384;
+
 static int fwd_tiles_per_cta(const Problem& P, int nt) {
+    if (P.window <= 0 || P.window > 2 * kBN) return 2;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -1074,6 +1092,11 @@ cudaError_t tc_fwd(const Problem& P, const void* q, const void* k, const void* v
             return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
         return launch_fwd_tiles<1>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     }
+    // Causal rows of up to kTwoTileMaxRows: two row tiles per CTA in the
+    // multi-tile kernel. Longer rows make a two-tile CTA long enough that the
+    // launch's tail grows more than the shared start-up saves.
+    if (P.causal && pair && P.max_seqlen <= kTwoTileMaxRows && launch_regs_ok(fwd_tc_tiles_kernel<2>))
+        return launch_fwd_tiles<2>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     if (pair && launch_regs_ok(fwd_tc_kernel<2, 64>))
         return launch_fwd<2, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
     return launch_fwd<1, 64>(P, mq, mk, mv, sinks, o, o_lo, lse, flags, st);
