@@ -21,7 +21,8 @@ stage (the backward main loop; against HBM when its arithmetic intensity is
 below the ridge point, as in the window layers), ``e2e`` (the same step with
 inputs copied in from pinned host memory and every output copied back each
 step, the copies overlapping the neighbouring steps' compute; the backward
-as one sink_attn_bwd_ex call, whose preparation runs inside it), ``clocks``
+as one sink_attn_bwd_ex call, whose preparation runs inside it; with the
+copy rate of the pinned buffers measured alone), ``clocks``
 sampled during the timed region and ``cpu_baseline`` (the oracle on the host
 cores, bounded sample).
 
@@ -547,10 +548,13 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
     current step computes (device buffers double-buffered, events order the
     reuse). Timed from the first copy in to the last copy out.
 
-    The backward is the one-call sink_attn_bwd_ex unless --overlap-e2e asks
-    for the preparation on the side stream: with the host copies in flight
-    the overlapped form's time varied from run to run (from 4.2 to 5.5 ms a
-    step on one GB300, against 4.245 ms every time for the one call)."""
+    The backward is the one-call sink_attn_bwd_ex (--overlap-e2e puts its
+    preparation on the side stream as the device-timed loop does). The step
+    is bound by the host link here: 742 MB of copies a step at about
+    190-200 GB/s each way take about as long as the 4 ms of compute, so the
+    overlapped preparation gains nothing, and a run whose host memory is
+    busy with other work comes out slower. copy_gbs_alone gives the link's
+    rate for these buffers, measured outside the timed region."""
     import attention_sink_softmax_gb300 as sa
     host_in = {n: prob_host[n].pin_memory() for n in ("q", "k", "v", "sinks", "dout")}
     outs0 = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dsinks": dsinks}
@@ -563,6 +567,26 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def copy_rate(stream_, pairs, nbytes):
+        # one set of copies alone (outside the timed region), best of three:
+        # the link's rate for these pinned buffers, to read the end-to-end
+        # time against
+        best = 0.0
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream_):
+                a.record(stream_)
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+                b.record(stream_)
+            b.synchronize()
+            best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+        return best
+
+    torch.cuda.synchronize(dev)
+    h2d_gbs = copy_rate(s_in, [(dev_in[1][n], t) for n, t in host_in.items()], h2d)
+    d2h_gbs = copy_rate(s_out, [(host_out[n], t) for n, t in dev_out[0].items()], d2h)
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
@@ -642,7 +666,8 @@ def run_e2e(args, ws, dev, stream, side, prob_host, q, k, v, sinks, dout, cu, p,
             "overlap": "copies in and out on their own streams, overlapping the neighbouring steps' compute",
             "bwd": ("sink_attn_bwd_prepare on the side stream, then sink_attn_bwd_main"
                     if args.overlap_e2e and not args.serial_prepare and "o_lo" in dev_out[0]
-                    else "one sink_attn_bwd call")}
+                    else "one sink_attn_bwd call"),
+            "copy_gbs_alone": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
 
@@ -953,7 +978,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--overlap-e2e", action="store_true",
                     help="end-to-end timing with the backward's preparation on the side stream "
-                         "(default: the one-call backward)")
+                         "(default: the one-call backward; the host link bounds that step)")
     ap.add_argument("--serial-prepare", action="store_true",
                     help="run the backward preparation inside sink_attn_bwd_main on the step's "
                          "stream instead of beside the forward on a lower-priority one")
