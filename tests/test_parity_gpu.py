@@ -49,7 +49,7 @@ def test_tiny_fp32_workload_full_oracle():
 
 CASES = [
     # lengths, h_q, h_kv, packed, causal, window
-    ([300, 300], 8, 2, False, True, 0),        # padded, 3 tiles + ragged tail
+    ([300, 300], 8, 2, False, True, 0),        # padded, 3 tiles + ragged tail (a 1-tile CTA)
     ([1, 127, 129, 255, 300], 4, 1, True, True, 0),
     ([517], 8, 8, True, True, 128),            # MHA, window 128
     ([640, 33], 8, 1, True, True, 1),          # MQA, window 1 (diagonal only)
@@ -61,7 +61,8 @@ CASES = [
     ([900, 260], 14, 2, True, True, 640),      # group of 7, window 640
     ([700, 301], 6, 2, True, True, 256),       # window 256 (the multi-tile forward's limit), group of 3
     ([513, 129], 8, 2, True, True, 256),       # window 256, pairs of query heads, ragged tails
-    ([600, 77], 8, 2, True, True, 257),        # just above it: the one-tile forward with a window
+    ([600, 77], 8, 2, True, True, 257),        # just above it: two row tiles per CTA, both bounds
+    ([2100, 700, 3], 4, 2, True, True, 0),     # causal pairs: 17 row tiles, one CTA of one tile
 ]
 
 
