@@ -42,6 +42,13 @@
 // of 128 rows x 64 (128-byte rows), each filled by its own TMA box; S takes
 // D/16 K steps across the atoms, and P V is one N = D product per K step.
 // At D = 128 a CTA holds one tile (NT = 1): S 128 + O 128 + P 64 columns.
+//
+// Two kernels share this structure. fwd_tc_kernel runs one row tile per
+// query head of the CTA. fwd_tc_tiles_kernel (causal layers, D = 64) runs
+// several consecutive row tiles per CTA, a count chosen per launch (two
+// without a short window, 4 to 16 with a window of at most 256 keys); it
+// writes each whole tile's O and o_lo through shared memory with one TMA
+// store each, and tests per key block only the mask bound that can cut in.
 #include <cudaTypedefs.h>
 
 #include <cstring>
