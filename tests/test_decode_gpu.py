@@ -52,6 +52,8 @@ CASES = [
     ([300, 77], 32, 1),       # group of 32: the CUDA-core kernel for bf16 too
     ([77, 1500], 12, 1),      # group of 12: two 8-head blocks, four of them padding
     ([250, 3], 6, 2),         # group of 3
+    ([700, 5, 2100], 64, 8),  # the served model's 64 / 8 heads, ragged contexts
+    ([333, 90], 10, 5),       # 5 key/value heads (5 warps), group of 2
 ]
 
 
