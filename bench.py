@@ -700,6 +700,15 @@ def check_step_outputs(sa, p, q, k, v, sinks, dout, cu, o, lse, dq, dk, dv, dsin
         raise RuntimeError("timed step's dq differs from a one-stream step")
 
 
+def overlaps_preparation(serial_prepare: bool, window: int) -> bool:
+    """Whether the step issues the backward's preparation beside the forward
+    on the lower-priority stream. Only where the forward outlasts it: on the
+    window-128 layers the one-stream order measured faster (1.293 -> 1.276 ms
+    at B 4 x N 8192; 8.27 -> 7.96 ms on the 48 packed sequences), the short
+    forward leaving the preparation to run into the preprocess."""
+    return not serial_prepare and not (0 < window <= 256)
+
+
 def run_gpu(args, w, window):
     import attention_sink_softmax_gb300 as sa
 
@@ -730,12 +739,7 @@ def run_gpu(args, w, window):
 
     bwd_done = torch.cuda.Event()
     bwd_done.record(stream)
-    # The preparation overlaps the forward only where the forward outlasts it.
-    # On the window-128 layers the one-stream order measured faster
-    # (1.293 -> 1.276 ms at B 4 x N 8192; 8.27 -> 7.96 ms on the 48 packed
-    # sequences): the short forward leaves the preparation to run into the
-    # preprocess.
-    overlap = not args.serial_prepare and not (0 < window <= 256)
+    overlap = overlaps_preparation(args.serial_prepare, window)
 
     def step(ev=None):
         if ev is not None:

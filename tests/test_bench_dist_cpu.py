@@ -135,3 +135,15 @@ def test_spawn_ranks_reports_a_failing_rank(tmp_path):
     script = tmp_path / "fail.py"
     script.write_text("import os, sys\nsys.exit(3 if os.environ['RANK'] == '1' else 0)\n")
     assert bench.spawn_ranks(2, [sys.executable, str(script)]) == 3
+
+
+def test_preparation_overlaps_the_forward_only_without_a_short_window():
+    """The bench issues the backward's preparation beside the forward on full
+    causal layers and keeps it on the step's stream where a window of at most
+    256 keys makes the forward short; --serial-prepare keeps it there always."""
+    assert bench.overlaps_preparation(False, 0)
+    assert bench.overlaps_preparation(False, 257)
+    for window in (1, 128, 256):
+        assert not bench.overlaps_preparation(False, window)
+    for window in (0, 128, 4096):
+        assert not bench.overlaps_preparation(True, window)
