@@ -50,6 +50,7 @@ def test_tiny_fp32_workload_full_oracle():
 CASES = [
     # lengths, h_q, h_kv, packed, causal, window
     ([300, 300], 8, 2, False, True, 0),        # padded, 3 tiles + ragged tail (a 1-tile CTA)
+    ([512, 512], 4, 2, False, True, 0),        # padded, 4 whole tiles, two 2-tile CTAs per sequence
     ([1, 127, 129, 255, 300], 4, 1, True, True, 0),
     ([517], 8, 8, True, True, 128),            # MHA, window 128
     ([640, 33], 8, 1, True, True, 1),          # MQA, window 1 (diagonal only)
